@@ -1,0 +1,193 @@
+"""ctypes binding of libgdn_tree.so -- argument marshalling only.
+
+The functions carry the names of the C entry points declared in
+include/gdn_tree.h.  Every step of the computation runs in the CUDA library;
+this module only turns tensors into pointers and statuses into exceptions.  If
+the library has not been built, loading it raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from .build import LIB_PATH
+
+c_i32 = ctypes.c_int32
+c_p = ctypes.c_void_p
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_INVALID_TREE = -2
+GDN_ERR_INVALID_PATH = -3
+GDN_ERR_UNSUPPORTED = -4
+GDN_ERR_CUDA = -5
+GDN_ERR_CAPACITY = -7
+GDN_ERR_STATE = -8
+GDN_ERR_SCHEDULE = -9
+GDN_DTYPE_F32 = 0
+GDN_DTYPE_BF16 = 1
+GDN_COMMIT_COMPACT = 1
+GDN_MAX_NODES = 64
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"gdn status {status}: {msg}")
+        self.status = status
+
+
+class gdn_dims(ctypes.Structure):
+    _fields_ = [("Hk", c_i32), ("Hv", c_i32), ("dk", c_i32), ("dv", c_i32), ("K", c_i32),
+                ("conv_mode", c_i32), ("act", c_i32), ("in_dtype", c_i32),
+                ("q_scale", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+
+
+_SCHED_ARRAYS = ["subtree", "heavy", "chain_of", "pos_in_chain", "chain_head", "chain_len", "chain_off",
+                 "chain_nodes", "chain_wave", "chain_src_slot", "wave_off", "boundary_slot", "boundary_node"]
+
+
+class gdn_schedule(ctypes.Structure):
+    _fields_ = [("n", c_i32), ("n_chains", c_i32), ("n_waves", c_i32), ("n_boundary", c_i32)] + \
+               [(name, ctypes.POINTER(c_i32)) for name in _SCHED_ARRAYS]
+
+
+class gdn_batch_schedule(ctypes.Structure):
+    _fields_ = [("B", c_i32), ("n_max", c_i32), ("nb_max", c_i32), ("words", c_p)]
+
+
+class gdn_banks(ctypes.Structure):
+    _fields_ = [("k", c_p * 2), ("u", c_p * 2), ("a", c_p * 2), ("x", c_p * 2),
+                ("pend_path", c_p), ("pend_len", c_p), ("err", c_p),
+                ("B", c_i32), ("layers", c_i32), ("n_max", c_i32),
+                ("write_bank", c_i32), ("pend_bank", c_i32), ("verified_bank", c_i32)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is not built; run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        L.gdn_abi_version.restype = c_i32
+        L.gdn_last_error.restype = ctypes.c_char_p
+        L.gdn_hld_schedule.argtypes = [P(c_i32), c_i32, P(gdn_schedule)]
+        L.gdn_schedule_words.argtypes = [c_i32]
+        L.gdn_schedule_words.restype = c_i32
+        L.gdn_pack_schedules.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
+        L.gdn_banks_init.argtypes = [P(gdn_banks), c_i32, c_i32, c_i32]
+        L.gdn_workspace_bytes.argtypes = [P(gdn_dims), c_i32, c_i32, c_i32]
+        L.gdn_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_tree_verify.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
+                                      c_p, P(gdn_banks), c_p, ctypes.c_size_t, c_p]
+        L.gdn_commit_fold.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_i32, P(gdn_banks), c_p]
+        L.gdn_finish.argtypes = [P(gdn_dims), c_i32, c_i32, c_p, c_p, P(gdn_banks), c_p]
+        L.gdn_check_error.argtypes = [P(gdn_banks), c_p]
+        for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_banks_init", "gdn_tree_verify",
+                     "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
+            getattr(L, name).restype = c_i32
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, lib().gdn_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gdn_abi_version() -> int:
+    return lib().gdn_abi_version()
+
+
+def gdn_last_error() -> str:
+    return lib().gdn_last_error().decode()
+
+
+def gdn_hld_schedule(parent) -> dict:
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    n = int(parent.shape[0])
+    size = max(n, 1) + 1
+    arrays = {name: np.full(size, -7, dtype=np.int32) for name in _SCHED_ARRAYS}
+    s = gdn_schedule()
+    for name in _SCHED_ARRAYS:
+        setattr(s, name, arrays[name].ctypes.data_as(ctypes.POINTER(c_i32)))
+    _check(lib().gdn_hld_schedule(parent.ctypes.data_as(ctypes.POINTER(c_i32)), n, ctypes.byref(s)))
+    lengths = dict(subtree=n, heavy=n, chain_of=n, pos_in_chain=n, chain_head=s.n_chains, chain_len=s.n_chains,
+                   chain_off=s.n_chains + 1, chain_nodes=n, chain_wave=s.n_chains, chain_src_slot=s.n_chains,
+                   wave_off=s.n_waves + 1, boundary_slot=n, boundary_node=s.n_boundary)
+    out = dict(n=s.n, n_chains=s.n_chains, n_waves=s.n_waves, n_boundary=s.n_boundary)
+    for name in _SCHED_ARRAYS:
+        out[name] = arrays[name][:lengths[name]].tolist()
+    return out
+
+
+def gdn_schedule_words(n_max: int) -> int:
+    return lib().gdn_schedule_words(n_max)
+
+
+def gdn_pack_schedules(parents: np.ndarray, n: np.ndarray):
+    """parents [B, n_max] int32 (rows padded with anything past n[b]), n [B] -> (words [B, W] int32, nb_max)."""
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    n = np.ascontiguousarray(n, dtype=np.int32)
+    B, n_max = parents.shape
+    words = np.empty((B, gdn_schedule_words(n_max)), dtype=np.int32)
+    nb = c_i32(0)
+    P = ctypes.POINTER(c_i32)
+    _check(lib().gdn_pack_schedules(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max,
+                                    words.ctypes.data_as(P), ctypes.byref(nb)))
+    return words, int(nb.value)
+
+
+def gdn_banks_init(banks: gdn_banks, B: int, layers: int, n_max: int):
+    _check(lib().gdn_banks_init(ctypes.byref(banks), B, layers, n_max))
+
+
+def gdn_workspace_bytes(dims: gdn_dims, B: int, layers: int, n_max: int) -> int:
+    return int(lib().gdn_workspace_bytes(ctypes.byref(dims), B, layers, n_max))
+
+
+def gdn_tree_verify(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, x_raw, conv_w, beta, log_g, state,
+                    conv_state, out_o, boundary_states, banks: gdn_banks, workspace, workspace_bytes: int,
+                    stream=None):
+    _check(lib().gdn_tree_verify(ctypes.byref(dims), layers, ctypes.byref(sched), _ptr(x_raw), _ptr(conv_w),
+                                 _ptr(beta), _ptr(log_g), _ptr(state), _ptr(conv_state), _ptr(out_o),
+                                 _ptr(boundary_states), ctypes.byref(banks), _ptr(workspace), workspace_bytes,
+                                 _stream(stream)))
+
+
+def gdn_commit_fold(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, path, length, flags: int,
+                    banks: gdn_banks, stream=None):
+    _check(lib().gdn_commit_fold(ctypes.byref(dims), layers, ctypes.byref(sched), _ptr(path), _ptr(length), flags,
+                                 ctypes.byref(banks), _stream(stream)))
+
+
+def gdn_finish(dims: gdn_dims, B: int, layers: int, state, conv_state, banks: gdn_banks, stream=None):
+    _check(lib().gdn_finish(ctypes.byref(dims), B, layers, _ptr(state), _ptr(conv_state), ctypes.byref(banks),
+                            _stream(stream)))
+
+
+def gdn_check_error(banks: gdn_banks, stream=None):
+    _check(lib().gdn_check_error(ctypes.byref(banks), _stream(stream)))

@@ -1,0 +1,245 @@
+/*
+ * gdn_tree.h -- C ABI for state-resident verification of speculative draft
+ * trees through Gated DeltaNet (gated delta-rule linear attention) layers.
+ *
+ * Method: "Lucebox SpecLA 与 Gated DeltaNet 状态驻留验证原理指南" (the SpecLA
+ * article), sections "状态驻留验证" (state-resident verify), "链分解与依赖波
+ * HLD 调度" (heavy-light chains and dependency waves), "接受因子缓存" (factor
+ * banks), "延迟融合提交" (deferred fused commit); and the Luce DFlash README,
+ * "How it works" (DDTree tree verify, tree-aware conv window).
+ *
+ * Per v-head the recurrent state is stored transposed, T = S^T, as a row-major
+ * [d_k][d_v] fp32 tile.  One token (x, beta, a) advances (T, W) by
+ *   y   = depthwise causal conv of the K-row window [W; x] (or y = x), then SiLU (optional)
+ *   q,k = L2-normalised q and k heads of y (q scaled by q_scale), v = v heads of y
+ *   T  <- exp(a) * T;  p = T^T k;  u = beta (v - p);  T <- T + k u^T;  o = T^T q
+ * which is S' = g S (I - beta k k^T) + beta v k^T, o = S' q.  A draft tree is
+ * verified by giving every node the state reached along its own root path.
+ *
+ * Conventions for every call:
+ *  - The caller owns every buffer.  No call allocates device memory.
+ *  - Device calls are asynchronous on the given stream, never synchronise the
+ *    host, and never trap on the device.  Host-detectable errors (bad sizes,
+ *    NULL or misaligned pointers, invalid trees) return a negative status
+ *    before anything is launched; gdn_last_error() then describes it.
+ *  - Device-detectable errors (an accepted path that is not a root path of the
+ *    verified tree) set bits in the caller's device error words
+ *    (gdn_banks.err); gdn_check_error() reads and clears them.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Per-node arrays are indexed [request][layer][node][...] with a node stride
+ *    of n_max; nodes are numbered so that parent[i] < i (node 0 is the root).
+ *  - Channel order of a raw input row: [q (Hk*dk) | k (Hk*dk) | v (Hv*dv)],
+ *    head-major.  v-head h uses q/k head h / (Hv/Hk).
+ */
+#ifndef GDN_TREE_H
+#define GDN_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+#define GDN_MAX_NODES 64   /* largest tree (n_max) the kernels accept */
+#define GDN_MAX_TAPS 8     /* largest conv kernel K */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1,   /* a size, pointer or alignment is wrong */
+  GDN_ERR_INVALID_TREE = -2,  /* parent[] is not a tree in topological order */
+  GDN_ERR_INVALID_PATH = -3,  /* (device) an accepted path is not a root path */
+  GDN_ERR_UNSUPPORTED = -4,   /* a head size or mode this build has no kernel for */
+  GDN_ERR_CUDA = -5,          /* a CUDA launch or copy failed */
+  GDN_ERR_CAPACITY = -7,      /* a buffer is smaller than the call needs */
+  GDN_ERR_STATE = -8,         /* calls out of order (commit without a verify) */
+  GDN_ERR_SCHEDULE = -9       /* (device) packed schedule words out of range */
+} gdn_status;
+
+typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+/* Bits of gdn_banks.err[0]. err[1] holds 1 + the first request that set a bit. */
+#define GDN_DEVERR_INVALID_PATH 1  /* an accepted path is not a root path; nothing committed */
+#define GDN_DEVERR_SCHEDULE 2      /* packed schedule words out of range; the access was skipped */
+
+/* Shapes and modes of one GDN layer stack. */
+typedef struct {
+  int32_t Hk, Hv;      /* q/k heads and v-heads; Hv % Hk == 0 */
+  int32_t dk, dv;      /* head sizes: dk in {32, 64, 128}; dv in {32, 64, 128} */
+  int32_t K;           /* conv taps, 1..GDN_MAX_TAPS (ignored in bypass mode) */
+  int32_t conv_mode;   /* 0: y = x (inputs are q|k|v already); 1: causal depthwise conv */
+  int32_t act;         /* 0: none; 1: SiLU after the conv */
+  int32_t in_dtype;    /* gdn_dtype of x_raw, beta and log_g */
+  float q_scale;       /* multiplies the normalised q (1.0 gives o = S' q) */
+  float l2_eps;        /* q_hat = q / sqrt(sum q^2 + l2_eps); same for k */
+} gdn_dims;
+
+/* ---------------------------------------------------------------------------
+ * Heavy-light schedule of one tree (host, pure, O(n)).
+ * SpecLA article, "链分解与依赖波 HLD 调度": the heavy child of a node is its
+ * child with the largest subtree (ties: smaller index); heavy edges continue a
+ * chain and light edges start one; only the states at chain boundaries are
+ * materialised; chains are grouped into dependency waves.  Here the wave of a
+ * chain is the number of light edges from the root to its head, chains are
+ * ordered by (wave, head), boundary nodes are the parents of non-root chain
+ * heads (exactly the nodes with two or more children) and get slots in
+ * ascending node order.
+ *
+ * Every array is caller-owned with room for n entries (chain_off and wave_off:
+ * n + 1).  On GDN_ERR_INVALID_TREE nothing is written.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t n, n_chains, n_waves, n_boundary;
+  int32_t* subtree;        /* [n] subtree size of each node */
+  int32_t* heavy;          /* [n] heavy child, -1 for a leaf */
+  int32_t* chain_of;       /* [n] chain id of each node */
+  int32_t* pos_in_chain;   /* [n] position of each node in its chain */
+  int32_t* chain_head;     /* [n_chains] first node of each chain */
+  int32_t* chain_len;      /* [n_chains] */
+  int32_t* chain_off;      /* [n_chains + 1] offsets into chain_nodes */
+  int32_t* chain_nodes;    /* [n] chains concatenated, head to tail */
+  int32_t* chain_wave;     /* [n_chains] */
+  int32_t* chain_src_slot; /* [n_chains] boundary slot the chain starts from, -1 = persistent state */
+  int32_t* wave_off;       /* [n_waves + 1] chain-id ranges of each wave */
+  int32_t* boundary_slot;  /* [n] slot of a boundary node, -1 otherwise */
+  int32_t* boundary_node;  /* [n_boundary] node of each slot */
+} gdn_schedule;
+
+gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_schedule* out);
+
+/* ---------------------------------------------------------------------------
+ * Packed batch schedule: the compact form the kernels read.
+ * One record of gdn_schedule_words(n_max) int32 per request:
+ *   [0] n  [1] n_chains  [2] n_boundary  [3] n_waves
+ *   [4 .. 4+n_max)              parent (unused entries -1)
+ *   [4+n_max .. 4+2n_max)       boundary slot of each node (-1: none)
+ *   [4+2n_max .. 4+3n_max)      source slot of each chain in schedule order
+ *   [4+3n_max .. 5+4n_max)      chain offsets into the node list
+ *   [5+4n_max .. 5+5n_max)      nodes of the chains, concatenated
+ * gdn_pack_schedules runs gdn_hld_schedule on every request's tree and writes
+ * the records into words_host (B * gdn_schedule_words(n_max) int32, caller-
+ * owned host memory); *nb_max_out receives the largest boundary count.  The
+ * caller copies the words to the device and fills a gdn_batch_schedule.
+ * parents: B rows of n_max entries; n[b] nodes of request b are used.
+ * ------------------------------------------------------------------------- */
+int32_t gdn_schedule_words(int32_t n_max);
+gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
+                              int32_t* words_host, int32_t* nb_max_out);
+
+typedef struct {
+  int32_t B;               /* requests */
+  int32_t n_max;           /* node stride of every per-node array */
+  int32_t nb_max;          /* slot stride of boundary_states (>= every request's n_boundary) */
+  const int32_t* words;    /* device, B * gdn_schedule_words(n_max) int32 */
+} gdn_batch_schedule;
+
+/* ---------------------------------------------------------------------------
+ * Double-buffered FP32 factor banks (SpecLA article, "接受因子缓存": per node
+ * the normalised key, the delta-rule update vector u -- the "residual" that
+ * gives T <- g T + k u^T exactly --, the log-gate and the raw conv input; two
+ * banks alternate between "pending, consumed by the next verify" and "being
+ * written by this verify").
+ *
+ * Device buffers (caller-allocated, fp32):
+ *   k[i] [B][layers][n_max][Hk][dk]    u[i] [B][layers][n_max][Hv][dv]
+ *   a[i] [B][layers][n_max][Hv]        x[i] [B][layers][n_max][C]  (C = 2 Hk dk + Hv dv;
+ *                                           only read/written in conv_mode 1, may be NULL otherwise)
+ *   pend_path [B][n_max] int32, pend_len [B] int32: the accepted path recorded by
+ *   gdn_commit_fold; err [4] int32, zeroed by the caller before first use.
+ * Host fields (set by gdn_banks_init, then advanced by the calls):
+ *   write_bank: bank the next verify writes; pend_bank: bank holding the
+ *   committed-but-not-folded path (-1: none); verified_bank: bank written by
+ *   the last verify not yet committed (-1: none).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  float* k[2];
+  float* u[2];
+  float* a[2];
+  float* x[2];
+  int32_t* pend_path;
+  int32_t* pend_len;
+  int32_t* err;
+  int32_t B, layers, n_max;           /* capacity the buffers were sized for */
+  int32_t write_bank, pend_bank, verified_bank;
+} gdn_banks;
+
+gdn_status gdn_banks_init(gdn_banks* banks, int32_t B, int32_t layers, int32_t n_max);
+
+/* Workspace gdn_tree_verify needs (bytes): the normalised q and the v rows of
+ * every node, fp32.  Pass a device buffer of at least this size. */
+size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t n_max);
+
+/* ---------------------------------------------------------------------------
+ * gdn_tree_verify -- fold the pending path, then verify a batch of trees.
+ * SpecLA article, "延迟融合提交" and "状态驻留验证".
+ *
+ * If a committed path is pending (banks->pend_bank >= 0) its factors are first
+ * folded into each head's state tile as it is loaded -- T <- exp(a_t) T + k_t u_t^T
+ * along the path, and the conv window takes the path's last K-1 raw rows -- and
+ * the committed state and conv window are written back once.  Every node of
+ * every tree is then advanced from its parent's state; each chain of the
+ * heavy-light schedule keeps its tile on chip from head to tail.
+ *
+ *   x_raw      [B][layers][n_max][C]       in_dtype (bf16 or fp32)
+ *   conv_w     [layers][C][K]              fp32 (conv_mode 1; else may be NULL)
+ *   beta       [B][layers][n_max][Hv]      in_dtype
+ *   log_g      [B][layers][n_max][Hv]      in_dtype, a = log of the decay gate
+ *   state      [B][layers][Hv][dk][dv]     fp32 in/out: committed state (T = S^T)
+ *   conv_state [B][layers][K-1][C]         fp32 in/out: committed raw rows, oldest first (conv_mode 1)
+ *   out_o      [B][layers][n_max][Hv][dv]  fp32 out: o of every node
+ *   boundary_states [B][layers][nb_max][Hv][dk][dv] fp32 out: the state after each
+ *              boundary node, by slot.  May be NULL only if no tree has a boundary.
+ *   banks      factors of every node are written into bank write_bank
+ *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
+ * Rows of nodes >= n[b] are neither read nor written.
+ * ------------------------------------------------------------------------- */
+gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
+                           const void* x_raw, const float* conv_w, const void* beta, const void* log_g,
+                           float* state, float* conv_state, float* out_o, float* boundary_states,
+                           gdn_banks* banks, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gdn_commit_fold -- record the accepted path of the last verify as pending.
+ * SpecLA article, "延迟融合提交" and "接受因子缓存".
+ *
+ * path [B][sched->n_max] and len [B] are device int32 (so acceptance computed on
+ * the GPU needs no host round trip).  A valid path has path[0] = 0 and
+ * parent[path[i]] = path[i-1], 0 <= len <= n; len = 0 commits nothing.  The
+ * path is checked on the device: an invalid one commits nothing for that
+ * request and sets GDN_DEVERR_INVALID_PATH.  No state is touched: the fold
+ * happens in the next gdn_tree_verify (or gdn_finish), which reads the factors
+ * at the path's node indices, so no factor is copied whatever the path's shape.
+ * With flags & GDN_COMMIT_COMPACT the bank is also compacted in place into path
+ * order (slot i <- slot path[i]) and the recorded path becomes 0..len-1.
+ * Returns GDN_ERR_STATE if no verify happened since the last commit.
+ * ------------------------------------------------------------------------- */
+#define GDN_COMMIT_COMPACT 1
+gdn_status gdn_commit_fold(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
+                           const int32_t* path, const int32_t* len, int32_t flags,
+                           gdn_banks* banks, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gdn_finish -- materialise the pending path once (end of generation, switch to
+ * plain decoding, cancellation).  SpecLA article, "延迟融合提交"
+ * (finish_speculative_state).  Folds the pending factors into state and the
+ * pending raw rows into conv_state, exactly as the next verify would; a no-op
+ * when nothing is pending.
+ * ------------------------------------------------------------------------- */
+gdn_status gdn_finish(const gdn_dims* d, int32_t B, int32_t layers, float* state, float* conv_state,
+                      gdn_banks* banks, cudaStream_t stream);
+
+/* Synchronise the stream, read and clear banks->err.  Returns GDN_OK or the
+ * status of the first device error (GDN_ERR_INVALID_PATH). */
+gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream);
+
+/* Thread-local description of the last failed call on this thread. */
+const char* gdn_last_error(void);
+
+int32_t gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_TREE_H */

@@ -1,0 +1,191 @@
+"""Host-side checks of the C ABI library (no GPU needed).
+
+The library must load, export every function include/gdn_tree.h declares, give
+the oracle's heavy-light schedule bit for bit, pack it in the documented
+layout, and reject bad arguments before launching anything.  Calls here never
+reach a kernel launch: every argument set fails a host check first.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import gdn_oracle as O
+import synthetic as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def N():
+    from gated_deltanet_tree_gb300.build import build
+    build()
+    from gated_deltanet_tree_gb300 import _native
+    _native.lib()
+    return _native
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn_tree.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|size_t|int32_t|const char\s*\*)\s*(gdn_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_function(N):
+    names = declared_functions()
+    assert len(names) >= 11, names
+    lib = ctypes.CDLL(N.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in gdn_tree.h but not exported"
+    assert N.gdn_abi_version() == 1
+
+
+def _compare(N, parent):
+    got = N.gdn_hld_schedule(parent)
+    ref = O.hld_schedule(list(parent))
+    for key, val in ref.items():
+        assert got[key] == val, (key, list(parent))
+
+
+def test_hld_matches_oracle_on_every_small_tree(N):
+    for n in range(1, 9):
+        for parent in S.all_trees(n):
+            _compare(N, parent)
+
+
+def test_hld_matches_oracle_on_random_and_ddtrees(N):
+    rng = np.random.default_rng(2024)
+    for _ in range(10000):
+        _compare(N, S.random_tree(int(rng.integers(1, 65)), rng))
+    for seed in range(50):
+        _compare(N, S.ddtree(22, 4, 10, np.random.default_rng(seed)))
+        _compare(N, S.ddtree(64, 8, 16, np.random.default_rng(seed)))
+    _compare(N, S.chain_tree(64))
+
+
+def test_invalid_trees_rejected(N):
+    for bad in ([0], [-1, 1], [-1, 0, 3, 1], [-1, -1], [-1, 0, 0, 5], [-1, 0, -2]):
+        with pytest.raises(N.GdnError) as e:
+            N.gdn_hld_schedule(np.array(bad, dtype=np.int32))
+        assert e.value.status == N.GDN_ERR_INVALID_TREE
+    with pytest.raises(N.GdnError):
+        N.gdn_hld_schedule(np.zeros(0, dtype=np.int32))
+
+
+def test_packed_layout(N):
+    rng = np.random.default_rng(3)
+    n_max = 24
+    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(6)] + [S.ddtree(22, 4, 10, rng)]
+    P = np.full((len(trees), n_max), -1, dtype=np.int32)
+    n = np.array([len(t) for t in trees], dtype=np.int32)
+    for b, t in enumerate(trees):
+        P[b, :len(t)] = t
+    words, nb_max = N.gdn_pack_schedules(P, n)
+    assert words.shape == (len(trees), 5 + 5 * n_max)
+    assert nb_max == max(O.hld_schedule(list(t))["n_boundary"] for t in trees)
+    for b, t in enumerate(trees):
+        s = O.hld_schedule(list(t))
+        w = words[b]
+        m = len(t)
+        assert list(w[:4]) == [m, s["n_chains"], s["n_boundary"], s["n_waves"]]
+        assert list(w[4:4 + m]) == list(t)
+        assert list(w[4 + n_max:4 + n_max + m]) == s["boundary_slot"]
+        nc = s["n_chains"]
+        assert list(w[4 + 2 * n_max:4 + 2 * n_max + nc]) == s["chain_src_slot"]
+        assert list(w[4 + 3 * n_max:5 + 3 * n_max + nc]) == s["chain_off"]
+        assert list(w[5 + 4 * n_max:5 + 4 * n_max + m]) == s["chain_nodes"]
+    with pytest.raises(N.GdnError) as e:
+        N.gdn_pack_schedules(np.full((1, 65), -1, dtype=np.int32), np.array([3], dtype=np.int32))
+    assert e.value.status == N.GDN_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# argument checks of the device calls, all failing before any launch
+# ---------------------------------------------------------------------------
+
+FAKE = 1 << 20          # aligned, never dereferenced: every call below fails a host check first
+
+
+def _setup(N, **dims_kw):
+    kw = dict(Hk=2, Hv=4, dk=32, dv=32, K=4, conv_mode=1, act=1, in_dtype=0, q_scale=1.0, l2_eps=1e-6)
+    kw.update(dims_kw)
+    d = N.gdn_dims(**kw)
+    banks = N.gdn_banks()
+    for i in range(2):
+        banks.k[i] = banks.u[i] = banks.a[i] = banks.x[i] = FAKE
+    banks.pend_path = banks.pend_len = banks.err = FAKE
+    N.gdn_banks_init(banks, 1, 1, 8)
+    sched = N.gdn_batch_schedule(B=1, n_max=8, nb_max=2, words=FAKE)
+    return d, banks, sched
+
+
+def _verify(N, d, banks, sched, ws_bytes=None, **ptrs):
+    p = dict(x_raw=FAKE, conv_w=FAKE, beta=FAKE, log_g=FAKE, state=FAKE, conv_state=FAKE, out_o=FAKE,
+             boundary_states=FAKE, workspace=FAKE)
+    p.update(ptrs)
+    if ws_bytes is None:
+        ws_bytes = N.gdn_workspace_bytes(d, 1, 1, 8) - 1      # always one byte short unless a test says otherwise
+    return N.gdn_tree_verify(d, 1, sched, p["x_raw"], p["conv_w"], p["beta"], p["log_g"], p["state"],
+                             p["conv_state"], p["out_o"], p["boundary_states"], banks, p["workspace"], ws_bytes,
+                             stream=0)
+
+
+def _status(fn):
+    from gated_deltanet_tree_gb300._native import GdnError
+    try:
+        fn()
+    except GdnError as e:
+        return e.status
+    return 0
+
+
+def test_verify_rejects_bad_arguments(N):
+    d, banks, sched = _setup(N)
+    # the complete, well-formed argument set still stops at the 1-byte-short workspace
+    assert _status(lambda: _verify(N, d, banks, sched)) == N.GDN_ERR_CAPACITY
+    assert "workspace" in N.gdn_last_error()
+    assert _status(lambda: _verify(N, d, banks, sched, x_raw=None)) == N.GDN_ERR_INVALID_ARG
+    assert _status(lambda: _verify(N, d, banks, sched, state=FAKE + 4)) == N.GDN_ERR_INVALID_ARG
+    assert "aligned" in N.gdn_last_error()
+    assert _status(lambda: _verify(N, d, banks, sched, boundary_states=None)) == N.GDN_ERR_INVALID_ARG
+    for bad in (dict(dk=48), dict(dv=256), dict(K=9)):
+        d2, b2, s2 = _setup(N, **bad)
+        assert _status(lambda: _verify(N, d2, b2, s2)) == N.GDN_ERR_UNSUPPORTED, bad
+    for bad in (dict(Hv=5), dict(conv_mode=2), dict(act=3), dict(in_dtype=7), dict(l2_eps=-1.0)):
+        d2, b2, s2 = _setup(N, **bad)
+        assert _status(lambda: _verify(N, d2, b2, s2)) == N.GDN_ERR_INVALID_ARG, bad
+    # banks sized for another batch
+    d2, b2, s2 = _setup(N)
+    N.gdn_banks_init(b2, 2, 1, 8)
+    assert _status(lambda: _verify(N, d2, b2, s2)) == N.GDN_ERR_CAPACITY
+    # schedule with too many nodes
+    s3 = N.gdn_batch_schedule(B=1, n_max=65, nb_max=0, words=FAKE)
+    assert _status(lambda: _verify(N, d, banks, s3)) == N.GDN_ERR_UNSUPPORTED
+    # bypass mode does not need conv pointers, but still checks the rest
+    d4, b4, s4 = _setup(N, conv_mode=0, act=0)
+    assert _status(lambda: _verify(N, d4, b4, s4, conv_w=None, conv_state=None)) == N.GDN_ERR_CAPACITY
+
+
+def test_commit_and_finish_lifecycle_checks(N):
+    d, banks, sched = _setup(N)
+    st = _status(lambda: N.gdn_commit_fold(d, 1, sched, FAKE, FAKE, 0, banks, stream=0))
+    assert st == N.GDN_ERR_STATE                         # no verify since the last commit
+    st = _status(lambda: N.gdn_commit_fold(d, 1, sched, FAKE, FAKE, 4, banks, stream=0))
+    assert st == N.GDN_ERR_INVALID_ARG                   # unknown flag
+    st = _status(lambda: N.gdn_commit_fold(d, 1, sched, None, FAKE, 0, banks, stream=0))
+    assert st == N.GDN_ERR_INVALID_ARG
+    # finish with nothing pending is a no-op that touches nothing
+    assert _status(lambda: N.gdn_finish(d, 1, 1, FAKE, FAKE, banks, stream=0)) == 0
+    banks.pend_bank = 0                                  # inconsistent with write_bank = 0
+    assert _status(lambda: N.gdn_finish(d, 1, 1, FAKE, FAKE, banks, stream=0)) == N.GDN_ERR_STATE
+    with pytest.raises(N.GdnError):
+        N.gdn_banks_init(banks, 0, 1, 8)
+
+
+def test_workspace_bytes(N):
+    d = N.gdn_dims(Hk=16, Hv=48, dk=128, dv=128, K=4, conv_mode=1, act=1, in_dtype=1, q_scale=1.0, l2_eps=1e-6)
+    got = N.gdn_workspace_bytes(d, 32, 48, 22)
+    rows = 32 * 48 * 22
+    assert got >= rows * (16 * 128 + 48 * 128) * 4 and got % 256 == 0

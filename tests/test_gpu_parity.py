@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every case compares element by element on seeded inputs -- outputs of every
+node, boundary states, the factor bank written by the verify, the committed
+state and conv window after each fold, and the state after finish -- with the
+tolerances of tests/parity.py.  Full-size workloads are compared on sampled
+(request, layer) units that the oracle replays across all steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from parity import OracleUnit, check_factors, check_o, check_state
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gated_deltanet_tree_gb300.build import build
+    build()
+    import harness  # noqa: F401
+
+
+def _np(t):
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def run_parity(w, units=None, compact_steps=(), finish=True, plan=None):
+    """Run every step of workload w on the GPU; compare the chosen units with the oracle."""
+    from harness import GpuSession, WorkloadPlan
+    plan = plan or WorkloadPlan(w)
+    gs = GpuSession(w, plan)
+    if units is None:
+        units = [(b, l) for b in range(w.B) for l in range(w.layers)]
+    oracles = {u: OracleUnit(w, plan, *u) for u in units}
+    worst = dict(o=0.0, state=0.0, boundary=0.0)
+    for s in range(w.steps):
+        gs.verify(s)
+        bank = gs.ver.banks.verified_bank
+        torch.cuda.synchronize()
+        for (b, l), ou in oracles.items():
+            exp = ou.verify(s)
+            n = exp["n"]
+            worst["o"] = max(worst["o"], check_o(_np(gs.out_o[b, l, :n]), exp["o"], f"o step {s} unit {(b, l)}"))
+            worst["state"] = max(worst["state"], check_state(_np(gs.state[b, l]), exp["T"],
+                                                             f"committed state step {s} unit {(b, l)}"))
+            if w.conv_mode == 1 and w.K > 1:
+                np.testing.assert_allclose(_np(gs.conv_state[b, l]), exp["W"], rtol=0, atol=0,
+                                           err_msg=f"conv window step {s} unit {(b, l)}")
+            nb = exp["sched"]["n_boundary"]
+            worst["boundary"] = max(worst["boundary"], check_state(_np(gs.boundary[b, l, :nb]), exp["boundary"],
+                                                                   f"boundary step {s} unit {(b, l)}"))
+            xb = _np(gs.ver.bank_view("x", bank)[b, l]) if w.conv_mode == 1 else None
+            check_factors(_np(gs.ver.bank_view("k", bank)[b, l]), _np(gs.ver.bank_view("u", bank)[b, l]),
+                          _np(gs.ver.bank_view("a", bank)[b, l]), xb, exp, w.conv_mode)
+        compact = s in compact_steps
+        if compact:
+            pre = {f: gs.ver.bank_view(f, bank).clone() for f in (("k", "u", "a", "x") if w.conv_mode else ("k", "u", "a"))}
+        gs.commit(s, compact=compact)
+        if compact:
+            torch.cuda.synchronize()
+            for b in range(w.B):
+                path = plan.paths[s][b]
+                for f, t in pre.items():
+                    post = gs.ver.bank_view(f, bank)[b]
+                    assert torch.equal(post[:, :len(path)], t[b][:, torch.as_tensor(path, dtype=torch.long, device=t.device)]), f
+                    assert torch.equal(post[:, len(path):], t[b][:, len(path):]), f
+        for ou in oracles.values():
+            ou.commit(s)
+    if finish:
+        gs.finish()
+        torch.cuda.synchronize()
+        for (b, l), ou in oracles.items():
+            T, W = ou.committed()
+            check_state(_np(gs.state[b, l]), T, f"state after finish unit {(b, l)}")
+            if w.conv_mode == 1 and w.K > 1:
+                np.testing.assert_array_equal(_np(gs.conv_state[b, l]), W)
+    gs.ver.check_error()
+    return gs, worst
+
+
+# ---------------------------------------------------------------------------
+# small cases, every element
+# ---------------------------------------------------------------------------
+
+def test_tiny_conv_mode():
+    w = S.workload(1).replace(steps=4)
+    run_parity(w)
+
+
+def test_tiny_bypass_mode():
+    w = S.workload(1).replace(steps=4, conv_mode=0, act=0)
+    run_parity(w)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 32), (128, 32), (64, 128), (128, 128), (32, 32)])
+def test_head_shapes_and_gqa(dk, dv):
+    # d_k != d_v catches a transposed state; Hv = 3 Hk checks the v-head -> k-head map
+    w = S.workload(1).replace(Hk=2, Hv=6, dk=dk, dv=dv, steps=3, tree="random", budget=12, n_max=12, path_max=12)
+    run_parity(w)
+
+
+def test_ragged_batch_and_degenerate_trees():
+    # per-request tree sizes 1 .. n_max, a single-node tree, a full chain, L = 0 and L = n commits
+    n_max = 16
+    w = S.workload(1).replace(B=5, layers=2, n_max=n_max, steps=3, tree="random", budget=n_max, path_max=n_max)
+    rng = np.random.default_rng(5)
+    trees, paths = [], []
+    for s in range(w.steps):
+        ts = [np.array([-1], dtype=np.int32), S.chain_tree(n_max), S.random_tree(7, rng), S.random_tree(n_max, rng),
+              S.random_tree(3, rng)]
+        ps = [np.array([0], dtype=np.int32), np.arange(n_max, dtype=np.int32), np.zeros(0, dtype=np.int32),
+              S.random_walk_path(ts[3], rng, max_len=n_max), S.random_walk_path(ts[4], rng, max_len=3)]
+        trees.append(ts)
+        paths.append(ps)
+    from harness import WorkloadPlan
+    run_parity(w, plan=WorkloadPlan(w, trees, paths))
+
+
+def test_compaction_is_exact_and_transparent():
+    w = S.workload(1).replace(B=3, layers=2, steps=4, tree="random", budget=10, n_max=10, path_max=10)
+    gs, _ = run_parity(w, compact_steps=(0, 1, 2, 3))
+
+
+def test_qwen_like_single_layer():
+    w = S.workload(2).replace(steps=3)
+    run_parity(w)
+
+
+def test_chain64_single_layer():
+    # the pure-chain shape of the stress workload: 64-node chain, chain acceptance of the whole walk
+    w = S.workload(6).replace(B=2, layers=1, steps=2)
+    run_parity(w)
+
+
+def test_ddtree64_top8_single_layer():
+    w = S.workload(5).replace(B=2, layers=1, steps=2)
+    run_parity(w)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled units
+# ---------------------------------------------------------------------------
+
+def test_qwen_48_layers_commit_then_verify():
+    w = S.workload(3)
+    run_parity(w, units=[(0, 0), (0, 17), (0, 47)])
+
+
+def test_batched_32x48_eight_steps():
+    w = S.workload(4)
+    run_parity(w, units=[(0, 0), (13, 29), (31, 47)])
+
+
+# ---------------------------------------------------------------------------
+# lifecycle and device-side checks
+# ---------------------------------------------------------------------------
+
+def test_fold_reproduces_boundary_state_bitwise():
+    """The committed state folded from the factor bank equals, bit for bit, the
+    state the previous verify stored for the path's last node when that node was
+    a boundary (same operation order in fold and verify)."""
+    from harness import GpuSession, WorkloadPlan
+    w = S.workload(2).replace(steps=2)
+    plan = WorkloadPlan(w)
+    p0 = plan.trees[0][0]
+    kids = np.bincount(p0[1:], minlength=len(p0))
+    target = max(i for i in range(len(p0)) if kids[i] >= 2)
+    path = [target]
+    while p0[path[-1]] >= 0:
+        path.append(int(p0[path[-1]]))
+    plan.paths[0][0] = np.array(path[::-1], dtype=np.int32)
+    gs = GpuSession(w, plan)
+    gs.verify(0)
+    slot = sorted(i for i in range(len(p0)) if kids[i] >= 2).index(target)
+    saved = gs.boundary[0, 0, slot].clone()
+    gs.commit(0)
+    gs.verify(1)
+    torch.cuda.synchronize()
+    assert torch.equal(gs.state[0, 0], saved)
+
+
+def test_invalid_path_sets_device_error_and_commits_nothing():
+    from harness import GpuSession, WorkloadPlan
+    import gated_deltanet_tree_gb300 as G
+    w = S.workload(1).replace(B=2, steps=2, tree="random", budget=8, n_max=8)
+    plan = WorkloadPlan(w)
+    p = plan.trees[0][1]
+    non_child = [i for i in range(1, len(p)) if p[i] != 0]
+    # [0, v] with v not a child of the root, or (star tree) a path that does not start at the root
+    plan.paths[0][1] = np.array([0, non_child[0]] if non_child else [1], dtype=np.int32)
+    gs = GpuSession(w, plan)
+    state0 = gs.state.clone()
+    gs.verify(0)
+    gs.commit(0)
+    with pytest.raises(G.GdnError) as e:
+        gs.ver.check_error()
+    assert e.value.status == G._native.GDN_ERR_INVALID_PATH
+    assert int(gs.ver.pend_len[1]) == 0
+    gs.verify(1)
+    torch.cuda.synchronize()
+    assert torch.equal(gs.state[1], state0[1])       # nothing folded for the bad request
+    assert not torch.equal(gs.state[0], state0[0])   # the good request folded its path
+    gs.ver.check_error()
+
+
+def test_finish_without_pending_is_a_noop_and_commit_needs_verify():
+    from harness import GpuSession
+    import gated_deltanet_tree_gb300 as G
+    w = S.workload(1)
+    gs = GpuSession(w)
+    s0 = gs.state.clone()
+    gs.finish()
+    torch.cuda.synchronize()
+    assert torch.equal(gs.state, s0)
+    with pytest.raises(G.GdnError) as e:
+        gs.commit(0)
+    assert e.value.status == G._native.GDN_ERR_STATE
+
+
+def test_cuda_graph_replay_matches_eager():
+    from harness import GpuSession, WorkloadPlan
+    w = S.workload(2).replace(B=2, layers=3, steps=3)
+    plan = WorkloadPlan(w)
+    eager = GpuSession(w, plan)
+    graphed = GpuSession(w, plan)
+    for s in range(w.steps):
+        graphed.step_inputs(s), graphed.schedule(s), graphed.paths(s)
+    outs_e, outs_g = [], []
+    for s in range(w.steps):
+        eager.verify(s)
+        outs_e.append(eager.out_o.clone())
+        eager.commit(s)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for s in range(w.steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            graphed.verify(s, stream=stream)
+            graphed.commit(s, stream=stream)
+        g.replay()
+        torch.cuda.synchronize()
+        outs_g.append(graphed.out_o.clone())
+    for a, b in zip(outs_e, outs_g):
+        assert torch.equal(a, b)
+    assert torch.equal(eager.state, graphed.state)
