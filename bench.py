@@ -1,0 +1,449 @@
+"""Throughput of GDN tree verification with fused commit on one or more GPUs.
+
+A step is one pass of the whole path over one batch: heavy-light schedules of
+every request's tree on the host and their upload, the verify call (pending
+commit folded into the conv window and the state tiles, every node advanced,
+boundary states and factors written) and the commit of each request's
+accepted path.  Default workload: 32 requests x 48 GDN layers of 48 v-heads
+(d_k = d_v = 128, conv K = 4, bf16 inputs), a fresh 22-node top-4 DDTree per
+request and step, alternating factor banks.  The metric is verified tree nodes
+per second, one unit being one (request, GDN layer, v-head, node).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own batch of requests (weak scaling, no
+collective on the data path); timing is the max over ranks.  --impl reference
+times the CPU oracle on the host cores instead (a bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as S  # noqa: E402
+
+METRIC = "verified tree-nodes/sec (GDN layer·head·node) and achieved HBM GB/s vs GB300 peak"
+UNIT = "nodes/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes of one verify call (compulsory traffic: every input read
+# once, every output written once)
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(w: S.Workload, n_per_req, nb_per_req, pend_len_per_req):
+    """Compulsory bytes of one gdn_tree_verify call (conv window + chain verify)."""
+    ib = 2 if w.in_dtype == S.DTYPE_BF16 else 4
+    tile = w.dk * w.dv * 4 * w.Hv                    # all v-heads of one (request, layer)
+    C = w.C
+    total = 0
+    for n, nb, L in zip(n_per_req, nb_per_req, pend_len_per_req):
+        per_bl = tile                                 # state read
+        per_bl += tile if L > 0 else 0                # committed state written once
+        per_bl += nb * tile                           # boundary states written
+        per_bl += n * (C * ib + 2 * w.Hv * ib)        # x, beta, log_g read
+        per_bl += n * w.Hv * w.dv * 4                 # o written
+        per_bl += n * (w.Hk * w.dk + w.Hv * w.dv + w.Hv + (C if w.conv_mode else 0)) * 4   # factor bank written
+        if w.conv_mode and w.K > 1:
+            per_bl += (w.K - 1) * C * 4 * (2 if L > 0 else 1)   # conv window read (+ written when folded)
+            per_bl += min(L, w.K - 1) * C * 4                    # pending raw rows read
+        per_bl += L * (w.Hk * w.dk + w.Hv * w.dv + w.Hv) * 4     # pending factors read
+        total += per_bl * w.layers
+    if w.conv_mode:
+        total += w.layers * C * w.K * 4               # conv weights
+    return total
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/gdn_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# oracle baseline (CPU)
+# ----------------------------------------------------------------------------
+
+def _oracle_unit(args):
+    cfg_kw, b, l = args
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    sys.path.insert(0, ROOT)
+    import synthetic as S2
+    from oracle import gdn_oracle as O
+    w = S2.Workload(**cfg_kw)
+    parent = S2.tree_for(w, b, 0)
+    n = len(parent)
+    x, be, ag = S2.node_inputs(w, b, l, 0)
+    d = O.dims_of(w)
+    T = S2.init_state(w, b, l).astype(np.float64)
+    W = S2.init_conv_state(w, b, l).astype(np.float64)
+    cw = S2.conv_weight(w, l).astype(np.float64) if w.conv_mode else None
+    t0 = time.perf_counter()
+    O.verify_tree(T, W, parent, O.as_f64(x[:n], w.in_dtype), O.as_f64(be[:n], w.in_dtype),
+                  O.as_f64(ag[:n], w.in_dtype), cw, d)
+    return n * w.Hv, time.perf_counter() - t0
+
+
+def _warm_worker(_):
+    sys.path.insert(0, ROOT)
+    import synthetic  # noqa: F401
+    from oracle import gdn_oracle  # noqa: F401
+    return 0
+
+
+def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None):
+    """Oracle verify (one full root-path replay per node) on a sample of (request, layer) blocks."""
+    import dataclasses
+    cores = cores or os.cpu_count() or 1
+    kw = dataclasses.asdict(w)
+    units = [(kw, b, l) for l in range(w.layers) for b in range(w.B)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(units))
+    ctx = mp.get_context("spawn")
+    done_units, blocks = 0, 0
+    with ctx.Pool(cores) as pool:
+        pool.map(_warm_worker, range(cores))      # spawn and imports are not timed
+        t0 = time.perf_counter()
+        pos = 0
+        while pos < len(order):
+            batch = [units[i] for i in order[pos:pos + cores]]
+            pos += len(batch)
+            for u, _ in pool.map(_oracle_unit, batch):
+                done_units += u
+                blocks += 1
+            if time.perf_counter() - t0 >= target_s:
+                break
+    dt = time.perf_counter() - t0
+    return {"value": done_units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{blocks} of {w.B * w.layers} (request, layer) blocks of step 0, all {w.Hv} v-heads and "
+                      f"every node, {dt:.1f} s wall on {cores} host processes (spawn pool)"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, w: S.Workload, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_tree_gb300 import _native as N
+    from harness import GpuSession, WorkloadPlan
+    from gated_deltanet_tree_gb300.runtime import paths_tensor
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    # every rank serves its own requests: request ids are offset by rank
+    plan_w = w
+    plan = WorkloadPlan(plan_w, trees=[[S.tree_for(w, b + rank * w.B, s) for b in range(w.B)]
+                                       for s in range(w.steps)])
+    plan.paths = [[S.path_for(w, plan.trees[s][b], b + rank * w.B, s) for b in range(w.B)] for s in range(w.steps)]
+    gs = GpuSession(w, plan, device=dev, preload_steps=range(w.steps))
+    stream = torch.cuda.current_stream(dev)
+    ver = gs.ver
+
+    # pinned host buffers for each step's packed schedule words (filled by the host HLD inside the timed loop)
+    words_dev = [torch.empty(w.B, N.gdn_schedule_words(w.n_max), dtype=torch.int32, device=dev)
+                 for _ in range(w.steps)]
+    words_host = [torch.empty(w.B, N.gdn_schedule_words(w.n_max), dtype=torch.int32).pin_memory()
+                  for _ in range(w.steps)]
+    parents_host = []
+    for s in range(w.steps):
+        P = np.full((w.B, w.n_max), -1, dtype=np.int32)
+        n = np.zeros(w.B, dtype=np.int32)
+        for b, p in enumerate(plan.trees[s]):
+            P[b, :len(p)] = p
+            n[b] = len(p)
+        parents_host.append((P, n))
+    paths = [gs.paths(s) for s in range(w.steps)]
+
+    def sched_struct(s):
+        return N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, words=words_dev[s].data_ptr())
+
+    def one_step(i, timing=None):
+        s = i % w.steps
+        P, n = parents_host[s]
+        words, _ = N.gdn_pack_schedules(P, n)                       # host heavy-light schedules
+        words_host[s].numpy()[...] = words
+        words_dev[s].copy_(words_host[s], non_blocking=True)
+        X, BE, AG = gs.inputs[s]
+        sc = sched_struct(s)
+        if timing is not None:
+            timing[0].record(stream)
+        N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
+                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+        if timing is not None:
+            timing[1].record(stream)
+        N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # bytes / units of each step (pending length of step s = accepted path length of step s-1)
+    units_per_step, bytes_per_step = [], []
+    for i in range(args.warmup + args.steps):
+        s = i % w.steps
+        n_req = [len(p) for p in plan.trees[s]]
+        nb_req = [int(N.gdn_hld_schedule(p)["n_boundary"]) for p in plan.trees[s]]
+        prev = plan.paths[(i - 1) % w.steps] if i > 0 else [[] for _ in range(w.B)]
+        L_req = [len(p) for p in prev]
+        units_per_step.append(sum(n_req) * w.layers * w.Hv)
+        bytes_per_step.append(algorithmic_bytes(w, n_req, nb_req, L_req))
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize(dev)
+    ver.check_error()
+
+    clocks = ClockSampler(dev.index)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for k in range(args.steps):
+        one_step(args.warmup + k, ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ver.check_error()
+    ms = t_start.elapsed_time(t_end)
+    verify_ms = [a.elapsed_time(b) for a, b in ev]
+
+    timed_units = sum(units_per_step[args.warmup:])
+    timed_bytes = bytes_per_step[args.warmup:]
+
+    # finish (materialise the last pending path) timed on its own
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    ver.finish(gs.state, gs.conv_state, stream)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    finish_ms = f0.elapsed_time(f1)
+
+    # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
+    if args.no_e2e:
+        e2e = dict(ms=float("nan"), units=0, steps=0, h2d=0, d2h=0)
+    else:
+        e2e = run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct,
+                      units_per_step)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e["ms"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+        u = torch.tensor([timed_units, e2e["units"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        timed_units_all, e2e_units_all = float(u[0]), float(u[1])
+    else:
+        e2e_ms = e2e["ms"]
+        timed_units_all, e2e_units_all = timed_units, e2e["units"]
+
+    peak, peak_kind = peaks()
+    avg_verify_s = statistics.mean(verify_ms) / 1e3
+    avg_bytes = statistics.mean(timed_bytes)
+    achieved = avg_bytes / avg_verify_s / 1e9
+    return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk,
+                achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
+                e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap,
+                gpu_launches=args.steps * 3)
+
+
+def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct, units_per_step):
+    import torch
+    from gated_deltanet_tree_gb300 import _native as N
+    steps = max(1, min(args.steps, 8))
+    nsrc = min(2, w.steps)
+    host_in = []
+    for s in range(nsrc):
+        X, BE, AG = gs.inputs[s]
+        host_in.append(tuple(t.cpu().pin_memory() for t in (X, BE, AG)))
+    o_host = torch.empty(gs.out_o.shape, dtype=gs.out_o.dtype).pin_memory()
+    X_d, BE_d, AG_d = (torch.empty_like(t) for t in gs.inputs[0])
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0]) + words_host[0].numel() * 4
+    d2h = o_host.numel() * o_host.element_size()
+    ver = gs.ver
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    units = 0
+    e0.record(stream)
+    for k in range(steps):
+        s = k % nsrc
+        P, n = parents_host[s]
+        words, _ = N.gdn_pack_schedules(P, n)
+        words_host[s].numpy()[...] = words
+        words_dev[s].copy_(words_host[s], non_blocking=True)
+        for dst, src in zip((X_d, BE_d, AG_d), host_in[s]):
+            dst.copy_(src, non_blocking=True)
+        sc = sched_struct(s)
+        N.gdn_tree_verify(gs.dims, w.layers, sc, X_d, gs.conv_w, BE_d, AG_d, gs.state, gs.conv_state, gs.out_o,
+                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+        N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
+        o_host.copy_(gs.out_o, non_blocking=True)
+        units += units_per_step[s]
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return dict(ms=ms, units=units, steps=steps, h2d=h2d, d2h=d2h)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--requests", type=int, default=None, help="override requests per GPU (smaller profiling case)")
+    ap.add_argument("--layers", type=int, default=None, help="override GDN layers (smaller profiling case)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = S.workload(args.workload)
+    if args.requests:
+        w = w.replace(B=args.requests)
+    if args.layers:
+        w = w.replace(layers=args.layers)
+    config = {"workload": w.name, "requests_per_gpu": w.B, "gdn_layers": w.layers, "Hk": w.Hk, "Hv": w.Hv,
+              "dk": w.dk, "dv": w.dv, "conv_K": w.K, "tree": f"{w.budget}-node top-{w.top_k} DDTree" if
+              w.tree == "ddtree" else f"{w.budget}-node {w.tree}", "steps_cycle": w.steps,
+              "l2": "inputs larger than L2 (state alone is %.1f GB)" % (w.B * w.layers * w.Hv * w.dk * w.dv * 4 / 1e9),
+              "parallelism": f"replicas x{args.gpus}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        base = oracle_throughput(w, target_s=max(10.0, min(60.0, 4.0 * args.steps)))
+        line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    from gated_deltanet_tree_gb300.build import build
+    if rank == 0:
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        build()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the spawn pool starts before the first GPU call of this process
+        cpu = oracle_throughput(w, target_s=args.cpu_seconds)
+
+    r = run_gpu(args, w, rank, world)
+    if rank != 0:
+        return
+    value = r["units"] / (r["ms"] / 1e3)
+    e2e = r["e2e"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (bf16 inputs)", "data": "synthetic (seeded DDTree-shaped trees, "
+        "random activations; no model weights)", "config": config,
+        "roofline": {"bound": "hbm", "kernel": "gdn_tree_verify (conv_window_kernel + chain_verify_kernel)",
+                     "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                     "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
+                     "algorithmic_bytes_per_launch": r["avg_bytes"],
+                     "avg_launch_ms": statistics.mean(r["verify_ms"]), "traffic": None},
+        "finish_ms": r["finish_ms"],
+        "clocks": r["clocks"],
+        "e2e": None if args.no_e2e else {
+            "value": r["e2e_units"] / (r["e2e_ms"] / 1e3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
+        "gpu_launches": r["gpu_launches"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
