@@ -86,11 +86,13 @@ def lib():
         L.gdn_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_tree_verify.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
                                       c_p, P(gdn_banks), c_p, ctypes.c_size_t, c_p]
+        L.gdn_tree_verify_noalloc.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_p, c_p, c_p,
+                                              c_p, c_p, c_p, P(gdn_banks), c_p]
         L.gdn_commit_fold.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_i32, P(gdn_banks), c_p]
         L.gdn_finish.argtypes = [P(gdn_dims), c_i32, c_i32, c_p, c_p, P(gdn_banks), c_p]
         L.gdn_check_error.argtypes = [P(gdn_banks), c_p]
         for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_banks_init", "gdn_tree_verify",
-                     "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
+                     "gdn_tree_verify_noalloc", "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
             getattr(L, name).restype = c_i32
         _lib = L
     return _lib
@@ -176,6 +178,14 @@ def gdn_tree_verify(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, x_ra
                                  _ptr(beta), _ptr(log_g), _ptr(state), _ptr(conv_state), _ptr(out_o),
                                  _ptr(boundary_states), ctypes.byref(banks), _ptr(workspace), workspace_bytes,
                                  _stream(stream)))
+
+
+def gdn_tree_verify_noalloc(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, x_raw, conv_w, beta, log_g,
+                            state, conv_state, out_o, boundary_states, banks: gdn_banks, stream=None):
+    """gdn_tree_verify without a workspace: the library's fixed device scratch is used instead."""
+    _check(lib().gdn_tree_verify_noalloc(ctypes.byref(dims), layers, ctypes.byref(sched), _ptr(x_raw), _ptr(conv_w),
+                                         _ptr(beta), _ptr(log_g), _ptr(state), _ptr(conv_state), _ptr(out_o),
+                                         _ptr(boundary_states), ctypes.byref(banks), _stream(stream)))
 
 
 def gdn_commit_fold(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, path, length, flags: int,

@@ -201,6 +201,31 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
                            gdn_banks* banks, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_tree_verify_noalloc -- gdn_tree_verify without a workspace argument, for
+ * callers that cannot allocate device memory where they verify: code running
+ * during stream capture (cudaMalloc is not allowed there), engines whose whole
+ * device pool belongs to their own allocator, plugins given only buffers and a
+ * stream.  The SpecLA article has no counterpart; this is a convenience of this
+ * library.
+ *
+ * Same arguments, semantics and errors as gdn_tree_verify, except that the
+ * q/v scratch lives in a fixed array inside the library: GDN_NOALLOC_SCRATCH_BYTES
+ * on every GPU that loads the library, kept until the process exits.  A batch
+ * whose gdn_workspace_bytes exceeds it is rejected with GDN_ERR_CAPACITY before
+ * anything runs (Qwen-like heads: B * layers * n_max <= 2047).  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current, so make it outside any stream capture and with the stream's
+ * device current.  Every call shares the array: calls whose kernels may overlap
+ * on the GPU race and must be serialised by the caller.  Nothing in the array
+ * needs clearing: every scratch row read is written earlier in the same call.
+ * ------------------------------------------------------------------------- */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_tree_verify_noalloc(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
+                                   const void* x_raw, const float* conv_w, const void* beta, const void* log_g,
+                                   float* state, float* conv_state, float* out_o, float* boundary_states,
+                                   gdn_banks* banks, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gdn_commit_fold -- record the accepted path of the last verify as pending.
  * SpecLA article, "延迟融合提交" and "接受因子缓存".
  *
