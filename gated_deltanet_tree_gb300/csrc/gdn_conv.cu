@@ -6,10 +6,17 @@
 // "状态驻留验证" (ggml_ssm_conv_specla) and "延迟融合提交" (the pending path's raw
 // rows are folded into the committed window before the verify reads it).
 //
-// One CTA per (request, layer, channel group); a group is one q head, one k head
-// or one v head, one thread per channel.  Every thread owns one channel of the
-// committed window, so the fold and the write-back need no synchronisation; the
-// only block-wide step is the sum of squares for the q/k normalisation.
+// One CTA per (request, layer, group of whole heads of one kind -- q, k or v --
+// spanning at most 256 channels); every thread owns two adjacent channels, so
+// loads of the raw rows are 4-byte (bf16) or 8-byte (fp32) per lane and
+// coalesced.
+//   phase 1: fold the pending raw rows into the committed window (each thread
+//            owns its channels' window, so the write-back needs no barrier);
+//            for every node build the window along the parent chain, convolve,
+//            apply the activation, keep y in shared memory, copy the raw row
+//            into the factor bank;
+//   phase 2: one warp per (node, head): sum of squares, normalise q and k,
+//            write q_hat / k_hat / v with 16-byte stores.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -18,134 +25,191 @@ namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 128;
+constexpr int kConvChannels = 2 * kConvThreads;   // channels per CTA
 
 template <typename InT>
-__device__ __forceinline__ float load_in(const InT* p, size_t i);
+struct Raw2;
 template <>
-__device__ __forceinline__ float load_in<float>(const float* p, size_t i) {
-  return __ldg(p + i);
-}
-template <>
-__device__ __forceinline__ float load_in<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
-  return __bfloat162float(p[i]);
-}
-
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();  // red[] may still be read by the previous call
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int w = 0; w < kConvThreads / 32; ++w) s += red[w];
-  return s;
-}
-
-template <typename InT>
-__global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p) {
-  __shared__ float red[kConvThreads / 32];
-  const int bl = blockIdx.x;                 // request * layers + layer
-  const int b = bl / p.layers, l = bl % p.layers;
-  const int grp = blockIdx.y;
-  const int nq = p.Hk * p.dk;
-  int kind, c0, width;                       // kind 0: q head, 1: k head, 2: v head
-  if (grp < p.Hk) {
-    kind = 0; c0 = grp * p.dk; width = p.dk;
-  } else if (grp < 2 * p.Hk) {
-    kind = 1; c0 = nq + (grp - p.Hk) * p.dk; width = p.dk;
-  } else {
-    kind = 2; c0 = 2 * nq + (grp - 2 * p.Hk) * p.dv; width = p.dv;
+struct Raw2<float> {
+  static __device__ __forceinline__ float2 load(const float* p, size_t i) {
+    return __ldg(reinterpret_cast<const float2*>(p + i));
   }
-  const int t = threadIdx.x;
-  const bool active = t < width;
-  const int c = c0 + (active ? t : 0);
-  const int K = p.K, C = p.C;
+};
+template <>
+struct Raw2<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 load(const __nv_bfloat16* p, size_t i) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + i));
+  }
+};
+
+// Head group of blockIdx.y: kind (0 q, 1 k, 2 v), first head, head count, head size.
+struct HeadGroup {
+  int kind, head0, heads, hsz, cbase;
+};
+__device__ __forceinline__ HeadGroup head_group(const ConvParams& p, int y) {
+  const int hq = kConvChannels / p.dk, hv = kConvChannels / p.dv;   // heads per group
+  const int gq = (p.Hk + hq - 1) / hq;
+  HeadGroup g;
+  if (y < 2 * gq) {
+    g.kind = y < gq ? 0 : 1;
+    const int yy = y - g.kind * gq;
+    g.head0 = yy * hq;
+    g.heads = min(hq, p.Hk - g.head0);
+    g.hsz = p.dk;
+    g.cbase = g.kind * p.Hk * p.dk + g.head0 * p.dk;
+  } else {
+    g.kind = 2;
+    g.head0 = (y - 2 * gq) * hv;
+    g.heads = min(hv, p.Hv - g.head0);
+    g.hsz = p.dv;
+    g.cbase = 2 * p.Hk * p.dk + g.head0 * p.dv;
+  }
+  return g;
+}
+
+// KT > 0 fixes the number of taps at compile time (window and taps stay in
+// registers); KT = 0 reads it from the parameters.
+template <typename InT, int KT>
+__global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p) {
+  extern __shared__ float2 ybuf[];             // [n_max][kConvThreads] pairs of channels
+  const int bl = blockIdx.x;                   // request * layers + layer
+  const int b = bl / p.layers, l = bl % p.layers;
+  const int tid = threadIdx.x;
+  const HeadGroup hg = head_group(p, blockIdx.y);
+  const int c = hg.cbase + 2 * tid;            // first of this thread's two channels
+  const bool active = 2 * tid < hg.heads * hg.hsz;
+  const int K = KT > 0 ? KT : p.K, C = p.C;
   const InT* x = static_cast<const InT*>(p.x_raw);
 
-  // Committed window of this channel, oldest row first.
-  float win[GDN_MAX_TAPS - 1];
-  float w[GDN_MAX_TAPS];
-  if (p.conv_mode == 1) {
+  // Committed window of the two channels, oldest row first.
+  float2 win[GDN_MAX_TAPS - 1];
+  if (p.conv_mode == 1 && active) {
     float* cs = p.conv_state + static_cast<size_t>(bl) * (K - 1) * C + c;
-    for (int j = 0; j < K - 1; ++j) win[j] = active ? cs[static_cast<size_t>(j) * C] : 0.f;
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) win[j] = *reinterpret_cast<const float2*>(cs + static_cast<size_t>(j) * C);
     if (p.fold) {
       const int L = p.pend_len[b];
       if (L > 0) {
         const int32_t* path = p.pend_path + static_cast<size_t>(b) * p.n_max;
         const float* px = p.pend_x + static_cast<size_t>(bl) * p.n_max * C + c;
         for (int i = (L > K - 1 ? L - (K - 1) : 0); i < L; ++i) {
+#pragma unroll
           for (int j = 0; j + 1 < K - 1; ++j) win[j] = win[j + 1];
-          if (K > 1) win[K - 2] = active ? px[static_cast<size_t>(path[i]) * C] : 0.f;
+          if (K > 1) win[K - 2] = *reinterpret_cast<const float2*>(px + static_cast<size_t>(path[i]) * C);
         }
-        if (active)
-          for (int j = 0; j < K - 1; ++j) cs[static_cast<size_t>(j) * C] = win[j];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) *reinterpret_cast<float2*>(cs + static_cast<size_t>(j) * C) = win[j];
       }
     }
   }
   if (p.words == nullptr) return;  // fold only
-  if (p.conv_mode == 1) {
-    const float* cw = p.conv_w + (static_cast<size_t>(l) * C + c) * K;
-    for (int j = 0; j < K; ++j) w[j] = active ? cw[j] : 0.f;
-  }
 
   const SchedLayout lay{p.n_max};
   const int32_t* rec = p.words + static_cast<size_t>(b) * lay.words();
   const int n = rec[0];
-  const int32_t* parent = rec + lay.parent();
   if (n < 1 || n > p.n_max) {
-    if (threadIdx.x == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+    if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
     return;
   }
+  const int32_t* parent = rec + lay.parent();
   const size_t xrow0 = static_cast<size_t>(bl) * p.n_max;   // row of node 0 of this (request, layer)
 
+  float2 w[GDN_MAX_TAPS];
+  if (p.conv_mode == 1 && active) {
+    const float* cw = p.conv_w + (static_cast<size_t>(l) * C + c) * K;
+#pragma unroll
+    for (int j = 0; j < K; ++j) w[j] = make_float2(cw[j], cw[K + j]);
+  }
+
+  // phase 1: conv + activation of every node
   for (int node = 0; node < n; ++node) {
-    const float xs = active ? load_in<InT>(x, (xrow0 + node) * C + c) : 0.f;
-    float y = xs;
-    if (p.conv_mode == 1) {
-      // tap K-1 multiplies the node itself, tap K-1-i its i-th predecessor on the
-      // root path; past the root the committed window supplies the rows.
-      y = w[K - 1] * xs;
-      int m = parent[node];
-      int ci = K - 2;
-      for (int i = 1; i < K; ++i) {
-        float xv;
-        if (m >= 0) {
-          xv = active ? load_in<InT>(x, (xrow0 + m) * C + c) : 0.f;
-          m = parent[m];
-          if (m >= node) m = -1;  // parents precede children; a corrupt entry ends the walk
-        } else {
-          xv = win[ci--];
+    float2 y = make_float2(0.f, 0.f);
+    if (active) {
+      const float2 xs = Raw2<InT>::load(x, (xrow0 + node) * C + c);
+      y = xs;
+      if (p.conv_mode == 1) {
+        // tap K-1 multiplies the node itself, tap K-1-i its i-th predecessor on the
+        // root path; past the root the committed window supplies the rows.
+        y.x = w[K - 1].x * xs.x;
+        y.y = w[K - 1].y * xs.y;
+        int m = parent[node];
+        int ci = K - 2;
+#pragma unroll
+        for (int i = 1; i < K; ++i) {
+          float2 xv;
+          if (m >= 0 && m < node) {
+            xv = Raw2<InT>::load(x, (xrow0 + m) * C + c);
+            m = parent[m];
+          } else {
+            // win[ci] with a register-resident window: select instead of a dynamic index
+            xv = win[0];
+#pragma unroll
+            for (int j = 1; j < GDN_MAX_TAPS - 1; ++j)
+              if (j < K - 1 && j == ci) xv = win[j];
+            --ci;
+            m = -1;
+          }
+          y.x = fmaf(w[K - 1 - i].x, xv.x, y.x);
+          y.y = fmaf(w[K - 1 - i].y, xv.y, y.y);
         }
-        y = fmaf(w[K - 1 - i], xv, y);
+        *reinterpret_cast<float2*>(p.x_out + (xrow0 + node) * C + c) = xs;
       }
-      if (active) p.x_out[(xrow0 + node) * C + c] = xs;
+      if (p.act == 1) {
+        y.x = y.x / (1.f + expf(-y.x));
+        y.y = y.y / (1.f + expf(-y.y));
+      }
     }
-    if (p.act == 1) y = y / (1.f + expf(-y));
+    ybuf[node * kConvThreads + tid] = y;
+  }
+  __syncthreads();
+
+  // phase 2: one warp per (node, head) -- normalise q and k, write q_hat, k_hat, v
+  const int lane = tid & 31, warp = tid >> 5;
+  const float* yb = reinterpret_cast<const float*>(ybuf);
+  const int kind = hg.kind, hsz = hg.hsz, head0 = hg.head0, heads = hg.heads;
+  for (int job = warp; job < n * heads; job += kConvThreads / 32) {
+    const int node = job / heads, hh = job % heads;
+    const float* yh = yb + node * kConvChannels + hh * hsz;
+    float scale = 1.f;
     if (kind < 2) {
-      const float ss = block_sum(active ? y * y : 0.f, red);
-      y = y * (1.f / sqrtf(ss + p.l2_eps));
-      if (kind == 0) {
-        y *= p.q_scale;
-        if (active) p.q_out[((xrow0 + node) * p.Hk + grp) * p.dk + t] = y;
-      } else if (active) {
-        p.k_out[((xrow0 + node) * p.Hk + (grp - p.Hk)) * p.dk + t] = y;
-      }
-    } else if (active) {
-      p.v_out[((xrow0 + node) * p.Hv + (grp - 2 * p.Hk)) * p.dv + t] = y;
+      float ss = 0.f;
+      for (int e = lane; e < hsz; e += 32) ss = fmaf(yh[e], yh[e], ss);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      scale = 1.f / sqrtf(ss + p.l2_eps);
+      if (kind == 0) scale *= p.q_scale;
+    }
+    float* dst;
+    if (kind == 0) dst = p.q_out + ((xrow0 + node) * p.Hk + head0 + hh) * p.dk;
+    else if (kind == 1) dst = p.k_out + ((xrow0 + node) * p.Hk + head0 + hh) * p.dk;
+    else dst = p.v_out + ((xrow0 + node) * p.Hv + head0 + hh) * p.dv;
+    for (int e = 4 * lane; e < hsz; e += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(yh + e);
+      *reinterpret_cast<float4*>(dst + e) = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
     }
   }
+}
+
+template <typename InT, int KT>
+cudaError_t launch_t(const ConvParams& p, cudaStream_t s) {
+  const int hq = kConvChannels / p.dk, hv = kConvChannels / p.dv;
+  dim3 grid(p.B * p.layers, 2 * ((p.Hk + hq - 1) / hq) + (p.Hv + hv - 1) / hv);
+  const size_t smem = p.words ? static_cast<size_t>(p.n_max) * kConvThreads * sizeof(float2) : 0;
+  auto k = conv_window_kernel<InT, KT>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k<<<grid, kConvThreads, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s) {
-  dim3 grid(p.B * p.layers, 2 * p.Hk + p.Hv);
   if (p.in_dtype == GDN_DTYPE_BF16)
-    conv_window_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, s>>>(p);
-  else
-    conv_window_kernel<float><<<grid, kConvThreads, 0, s>>>(p);
-  return cudaGetLastError();
+    return p.K == 4 ? launch_t<__nv_bfloat16, 4>(p, s) : launch_t<__nv_bfloat16, 0>(p, s);
+  return p.K == 4 ? launch_t<float, 4>(p, s) : launch_t<float, 0>(p, s);
 }
 
 }  // namespace gdn

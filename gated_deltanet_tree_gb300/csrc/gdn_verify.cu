@@ -10,13 +10,26 @@
 // Work unit: one CTA per (request, layer, v-head, column slice of d_v).  The CTA
 // walks every chain of its tree in schedule order (wave, head): the root chain
 // continues from the folded committed state; any other chain reloads the state
-// that a chain of an earlier wave stored at its boundary slot.  Each thread owns
-// one column of the slice and RPT = dk / TPC rows of it, so p = T^T k and
-// o = T^T q are in-thread sums plus (TPC = 2) one shuffle.  The per-node q/k of
-// the whole tree are staged in shared memory once.
+// that a chain of an earlier wave of the same CTA stored at its boundary slot.
 //
-// Arithmetic order is fixed so that the fold reproduces the verify bitwise:
-// both compute T <- fmaf(k, u, g * T) with the same u.
+// Thread layout: a thread owns RPT consecutive rows x 4 consecutive columns of
+// the [d_k][d_v] tile, held as packed (row r, row r+1) fp32 pairs so the tile
+// arithmetic issues as f32x2 instructions.  Lanes run along the columns first
+// (CG column groups), so each warp-wide 16-byte load or store of the tile reads
+// or writes whole 128-byte lines -- the layout that keeps the state and
+// boundary transfers cheap for the load/store pipe.  The reductions over d_k
+// (sk = T^T k, sq = T^T q) are in-thread sums, an xor-shuffle across the row
+// groups of one warp, and a sum over the warps through a small double-buffered
+// shared array (one barrier per node).  Per node:
+//   pass A (state before the node):  sk = T^T k,  sq = T^T q
+//   p = g sk,  u = beta (v - p),  o = g sq + u (k . q)          (= T'^T q exactly)
+//   pass B:  T <- fmaf(k, u, g * T)
+// Everything a node needs (k_hat, q_hat, v slice, gate, beta, k.q) is staged in
+// shared memory once per tree, and the pending path's factors once per chunk of
+// the fold, so the node loop issues no global loads.
+//
+// The fold applies the same pass B with the same u, so the committed state
+// reproduces, bit for bit, the state the earlier verify computed at that node.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -25,6 +38,31 @@ namespace gdn {
 namespace {
 
 constexpr int kVerifyThreads = 128;
+constexpr int kCols = 4;           // columns per thread
+constexpr int kFoldChunk = 16;     // pending nodes staged per fold step
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 pack2(float lo, float hi) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(u64 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 template <typename InT>
 __device__ __forceinline__ float load_in(const InT* p, size_t i);
@@ -37,12 +75,42 @@ __device__ __forceinline__ float load_in<__nv_bfloat16>(const __nv_bfloat16* p, 
   return __bfloat162float(p[i]);
 }
 
-template <int DK, int TPC, typename InT>
-__global__ void __launch_bounds__(kVerifyThreads) chain_verify_kernel(VerifyParams p, int cpb) {
-  constexpr int RPT = DK / TPC;             // rows of the tile per thread
-  static_assert(RPT % 4 == 0, "rows per thread must be a multiple of 4");
+// Shared-memory layout (floats): tree region, fold region, then the schedule record (int32).
+template <int DK>
+struct Smem {
+  int n_max, cpb;
+  __device__ int kq(int node) const { return node * 2 * DK; }                  // [n_max][2][DK]
+  __device__ int v(int node) const { return n_max * 2 * DK + node * cpb; }     // [n_max][cpb]
+  __device__ int g() const { return n_max * (2 * DK + cpb); }                  // [n_max] each
+  __device__ int beta() const { return g() + n_max; }
+  __device__ int a() const { return beta() + n_max; }
+  __device__ int kqdot() const { return a() + n_max; }
+  __device__ int fold0() const { return (kqdot() + n_max + 3) & ~3; }
+  __device__ int fk(int i) const { return fold0() + i * DK; }                   // [kFoldChunk][DK]
+  __device__ int fu(int i) const { return fold0() + kFoldChunk * DK + i * cpb; } // [kFoldChunk][cpb]
+  __device__ int fg() const { return fold0() + kFoldChunk * (DK + cpb); }      // [kFoldChunk]
+  __device__ int part0() const { return (fg() + kFoldChunk + 3) & ~3; }        // [2][warps][2][cpb]
+  __device__ int rec0(int warps) const { return part0() + 2 * warps * 2 * cpb; } // packed schedule record
+};
+
+template <int DK>
+size_t smem_bytes(int n_max, int cpb, int warps) {
+  const int fold0 = (n_max * (2 * DK + cpb) + 4 * n_max + 3) & ~3;
+  const int part0 = (fold0 + kFoldChunk * (DK + cpb) + kFoldChunk + 3) & ~3;
+  const int words = SchedLayout{n_max}.words();
+  return static_cast<size_t>(part0 + 2 * warps * 2 * cpb + words) * sizeof(float);
+}
+
+template <int DK, int RPT, int CPB, typename InT>
+__global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyParams p) {
+  constexpr int NP = RPT / 2;              // row pairs per column
+  constexpr int CG = CPB / kCols;          // column groups per CTA
+  constexpr int NW = (DK / RPT) * CG / 32; // warps per CTA
+  constexpr int cpb = CPB;
+  static_assert(RPT % 4 == 0 && CG <= 32 && (DK / RPT) * CG % 32 == 0, "layout");
   extern __shared__ float4 smem4[];
-  float* kq = reinterpret_cast<float*>(smem4);   // [n][2][DK]: k_hat then q_hat of every node
+  float* sm = reinterpret_cast<float*>(smem4);
+  const Smem<DK> L{p.n_max, cpb};
 
   const int slices = p.dv / cpb;
   int cta = blockIdx.x;
@@ -54,169 +122,282 @@ __global__ void __launch_bounds__(kVerifyThreads) chain_verify_kernel(VerifyPara
   const int b = cta / p.layers;
   const int bl = b * p.layers + l;
   const int kh = h / p.R;
+  const int tid = threadIdx.x;
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kColsPerWarp = 32 / TPC;
-  const int half = lane / kColsPerWarp;
-  const int col = s * cpb + warp * kColsPerWarp + (lane % kColsPerWarp);
-  const int row0 = half * RPT;
+  const int lane = tid & 31, warp = tid >> 5;
+  constexpr int nwarps = NW;
+  const int cg = tid % CG;                                         // column group
+  const int rg = tid / CG;                                         // row group
+  const int c0 = cg * kCols;                                       // first column within the slice
+  const int col = s * cpb + c0;                                    // first column within d_v
+  const int row0 = rg * RPT;
   const size_t tile = static_cast<size_t>(DK) * p.dv;
 
-  float T[RPT];
-  float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
+  // T[c][j] = (T[row0 + 2j][col + c], T[row0 + 2j + 1][col + c])
+  u64 T[kCols][NP];
+  auto load_tile = [&](const float* base) {
 #pragma unroll
-  for (int r = 0; r < RPT; ++r) T[r] = st[static_cast<size_t>(r) * p.dv];
-
-  // Deferred commit: T <- exp(a) T + k u^T along the pending path, gathered by node index.
-  if (p.fold) {
-    const int L = p.pend_len[b];
-    const int32_t* path = p.pend_path + static_cast<size_t>(b) * p.n_max;
-    for (int i = 0; i < L; ++i) {
-      const size_t row = static_cast<size_t>(bl) * p.n_max + path[i];
-      const float g = expf(p.pend_a[row * p.Hv + h]);
-      const float u = p.pend_u[(row * p.Hv + h) * p.dv + col];
-      const float4* k4 = reinterpret_cast<const float4*>(p.pend_k + (row * p.Hk + kh) * DK + row0);
+    for (int j = 0; j < NP; ++j) {
+      const float4 r0 = *reinterpret_cast<const float4*>(base + static_cast<size_t>(2 * j) * p.dv);
+      const float4 r1 = *reinterpret_cast<const float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv);
+      T[0][j] = pack2(r0.x, r1.x);
+      T[1][j] = pack2(r0.y, r1.y);
+      T[2][j] = pack2(r0.z, r1.z);
+      T[3][j] = pack2(r0.w, r1.w);
+    }
+  };
+  auto store_tile = [&](float* base) {
 #pragma unroll
-      for (int r4 = 0; r4 < RPT / 4; ++r4) {
-        const float4 kv = __ldg(k4 + r4);
-        T[4 * r4 + 0] = fmaf(kv.x, u, g * T[4 * r4 + 0]);
-        T[4 * r4 + 1] = fmaf(kv.y, u, g * T[4 * r4 + 1]);
-        T[4 * r4 + 2] = fmaf(kv.z, u, g * T[4 * r4 + 2]);
-        T[4 * r4 + 3] = fmaf(kv.w, u, g * T[4 * r4 + 3]);
+    for (int j = 0; j < NP; ++j) {
+      const float2 a0 = unpack2(T[0][j]), a1 = unpack2(T[1][j]), a2 = unpack2(T[2][j]), a3 = unpack2(T[3][j]);
+      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j) * p.dv) = make_float4(a0.x, a1.x, a2.x, a3.x);
+      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv) =
+          make_float4(a0.y, a1.y, a2.y, a3.y);
+    }
+  };
+  // pass B on every column: T <- fmaf(k, u_c, g * T)
+  auto update = [&](const float* kvec, float g, float4 u) {
+    const u64 g2 = pack2(g, g);
+    const u64 u2[kCols] = {pack2(u.x, u.x), pack2(u.y, u.y), pack2(u.z, u.z), pack2(u.w, u.w)};
+    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
+#pragma unroll
+    for (int j4 = 0; j4 < NP / 2; ++j4) {
+      const ulonglong2 kk = k4[j4];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        T[c][2 * j4 + 0] = fma2(kk.x, u2[c], mul2(g2, T[c][2 * j4 + 0]));
+        T[c][2 * j4 + 1] = fma2(kk.y, u2[c], mul2(g2, T[c][2 * j4 + 1]));
       }
     }
-    if (L > 0) {
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) st[static_cast<size_t>(r) * p.dv] = T[r];
-    }
-  }
-  if (p.words == nullptr) return;  // fold only
+  };
 
+  float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
+  load_tile(st);
+
+  // ---- schedule header
   const SchedLayout lay{p.n_max};
-  const int32_t* rec = p.words + static_cast<size_t>(b) * lay.words();
-  const int n = rec[0];
-  const int n_chains = rec[1];
-  if (n < 1 || n > p.n_max || n_chains < 1 || n_chains > n) {
-    if (threadIdx.x == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-    return;
+  const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
+  int n = 0, n_chains = 0;
+  int32_t* srec = reinterpret_cast<int32_t*>(sm + L.rec0(nwarps));
+  if (rec) {
+    n = rec[0];
+    n_chains = rec[1];
+    if (n < 1 || n > p.n_max || n_chains < 1 || n_chains > n) {
+      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+      return;
+    }
+    for (int i = tid; i < lay.words(); i += blockDim.x) srec[i] = rec[i];
   }
-  const int32_t* bslot = rec + lay.bslot();
-  const int32_t* csrc = rec + lay.chain_src();
-  const int32_t* coff = rec + lay.chain_off();
-  const int32_t* cnodes = rec + lay.chain_nodes();
 
-  // Stage k_hat and q_hat of every node of the tree.
-  {
-    const size_t nrow0 = static_cast<size_t>(bl) * p.n_max;
-    for (int idx = threadIdx.x; idx < n * (DK / 4); idx += blockDim.x) {
+  // ---- stage the tree: k_hat, q_hat (k-head kh), v slice, gate, beta of every node
+  const InT* beta = static_cast<const InT*>(p.beta);
+  const InT* logg = static_cast<const InT*>(p.log_g);
+  const size_t nrow0 = static_cast<size_t>(bl) * p.n_max;
+  if (rec) {
+    for (int idx = tid; idx < n * (DK / 4); idx += blockDim.x) {
       const int node = idx / (DK / 4), e4 = idx % (DK / 4);
       const size_t src = ((nrow0 + node) * p.Hk + kh) * DK;
-      smem4[(node * 2 + 0) * (DK / 4) + e4] = __ldg(reinterpret_cast<const float4*>(p.k_in + src) + e4);
-      smem4[(node * 2 + 1) * (DK / 4) + e4] = __ldg(reinterpret_cast<const float4*>(p.q_in + src) + e4);
+      smem4[L.kq(node) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.k_in + src) + e4);
+      smem4[(L.kq(node) + DK) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.q_in + src) + e4);
     }
+    for (int idx = tid; idx < n * (cpb / 4); idx += blockDim.x) {
+      const int node = idx / (cpb / 4), e4 = idx % (cpb / 4);
+      const size_t src = ((nrow0 + node) * p.Hv + h) * p.dv + s * cpb;
+      smem4[L.v(node) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.v_in + src) + e4);
+    }
+    for (int node = tid; node < n; node += blockDim.x) {
+      const float a = load_in<InT>(logg, (nrow0 + node) * p.Hv + h);
+      sm[L.a() + node] = a;
+      sm[L.g() + node] = expf(a);
+      sm[L.beta() + node] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
+    }
+  }
+
+  // ---- deferred commit: T <- exp(a) T + k u^T along the pending path, gathered by node index
+  const int Lp = p.fold ? p.pend_len[b] : 0;
+  const int32_t* path = p.pend_path + static_cast<size_t>(b) * p.n_max;
+  for (int f0 = 0; f0 < Lp; f0 += kFoldChunk) {
+    const int fn = min(kFoldChunk, Lp - f0);
+    if (f0 > 0) __syncthreads();   // previous chunk consumed
+    for (int idx = tid; idx < fn * (DK / 4); idx += blockDim.x) {
+      const int i = idx / (DK / 4), e4 = idx % (DK / 4);
+      const size_t row = nrow0 + path[f0 + i];
+      smem4[L.fk(i) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.pend_k + (row * p.Hk + kh) * DK) + e4);
+    }
+    for (int idx = tid; idx < fn * (cpb / 4); idx += blockDim.x) {
+      const int i = idx / (cpb / 4), e4 = idx % (cpb / 4);
+      const size_t row = nrow0 + path[f0 + i];
+      smem4[L.fu(i) / 4 + e4] =
+          __ldg(reinterpret_cast<const float4*>(p.pend_u + (row * p.Hv + h) * p.dv + s * cpb) + e4);
+    }
+    for (int i = tid; i < fn; i += blockDim.x) sm[L.fg() + i] = expf(p.pend_a[(nrow0 + path[f0 + i]) * p.Hv + h]);
+    __syncthreads();
+    for (int i = 0; i < fn; ++i)
+      update(sm + L.fk(i), sm[L.fg() + i], *reinterpret_cast<const float4*>(sm + L.fu(i) + c0));
+  }
+  if (Lp > 0) store_tile(st);
+  if (!rec) return;  // fold only
+  __syncthreads();   // tree staging complete
+
+  // ---- k . q of every node (one warp per node)
+  for (int node = warp; node < n; node += blockDim.x / 32) {
+    const float* kk = sm + L.kq(node);
+    float acc = 0.f;
+    for (int e = lane; e < DK; e += 32) acc = fmaf(kk[e], kk[DK + e], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sm[L.kqdot() + node] = acc;
   }
   __syncthreads();
 
-  const InT* beta = static_cast<const InT*>(p.beta);
-  const InT* logg = static_cast<const InT*>(p.log_g);
+  const int32_t* bslot = srec + lay.bslot();
+  const int32_t* csrc = srec + lay.chain_src();
+  const int32_t* coff = srec + lay.chain_off();
+  const int32_t* cnodes = srec + lay.chain_nodes();
   float* bnd_base = p.boundary + (static_cast<size_t>(bl) * p.nb_max * p.Hv + h) * tile +
                     static_cast<size_t>(row0) * p.dv + col;
+  int parity = 0;
   const size_t slot_stride = static_cast<size_t>(p.Hv) * tile;
+  const u64 zero2 = pack2(0.f, 0.f);
 
   for (int c = 0; c < n_chains; ++c) {
     const int src = csrc[c];
     const int i0 = coff[c], i1 = coff[c + 1];
     if (src >= p.nb_max || i0 < 0 || i1 > n || i0 > i1) {
-      if (threadIdx.x == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
       return;
     }
-    if (src >= 0) {
-      const float* bs = bnd_base + static_cast<size_t>(src) * slot_stride;
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) T[r] = bs[static_cast<size_t>(r) * p.dv];
-    }
+    if (src >= 0) load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
     for (int i = i0; i < i1; ++i) {
       const int node = cnodes[i];
       if (node < 0 || node >= n) {
-        if (threadIdx.x == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+        if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
         return;
       }
-      const size_t row = static_cast<size_t>(bl) * p.n_max + node;
-      const float a = load_in<InT>(logg, row * p.Hv + h);
-      const float bt = load_in<InT>(beta, row * p.Hv + h);
-      const float v = p.v_in[(row * p.Hv + h) * p.dv + col];
-      const float g = expf(a);
-      const float4* k4 = reinterpret_cast<const float4*>(kq + (node * 2 + 0) * DK + row0);
-      const float4* q4 = reinterpret_cast<const float4*>(kq + (node * 2 + 1) * DK + row0);
+      const float* kvec = sm + L.kq(node);
+      const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
+      const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(kvec + DK + row0);
 
-      float pk = 0.f;
+      // pass A on the state before this node
+      u64 ak[kCols], aq[kCols];
 #pragma unroll
-      for (int r4 = 0; r4 < RPT / 4; ++r4) {
-        const float4 kv = k4[r4];
-        T[4 * r4 + 0] = g * T[4 * r4 + 0];
-        T[4 * r4 + 1] = g * T[4 * r4 + 1];
-        T[4 * r4 + 2] = g * T[4 * r4 + 2];
-        T[4 * r4 + 3] = g * T[4 * r4 + 3];
-        pk = fmaf(T[4 * r4 + 0], kv.x, pk);
-        pk = fmaf(T[4 * r4 + 1], kv.y, pk);
-        pk = fmaf(T[4 * r4 + 2], kv.z, pk);
-        pk = fmaf(T[4 * r4 + 3], kv.w, pk);
-      }
-      if (TPC == 2) pk += __shfl_xor_sync(0xffffffffu, pk, kColsPerWarp);
-      const float u = bt * (v - pk);
-      float o = 0.f;
+      for (int cc = 0; cc < kCols; ++cc) ak[cc] = aq[cc] = zero2;
 #pragma unroll
-      for (int r4 = 0; r4 < RPT / 4; ++r4) {
-        const float4 kv = k4[r4];
-        const float4 qv = q4[r4];
-        T[4 * r4 + 0] = fmaf(kv.x, u, T[4 * r4 + 0]);
-        T[4 * r4 + 1] = fmaf(kv.y, u, T[4 * r4 + 1]);
-        T[4 * r4 + 2] = fmaf(kv.z, u, T[4 * r4 + 2]);
-        T[4 * r4 + 3] = fmaf(kv.w, u, T[4 * r4 + 3]);
-        o = fmaf(T[4 * r4 + 0], qv.x, o);
-        o = fmaf(T[4 * r4 + 1], qv.y, o);
-        o = fmaf(T[4 * r4 + 2], qv.z, o);
-        o = fmaf(T[4 * r4 + 3], qv.w, o);
+      for (int j4 = 0; j4 < NP / 2; ++j4) {
+        const ulonglong2 kk = k4[j4];
+        const ulonglong2 qq = q4[j4];
+#pragma unroll
+        for (int cc = 0; cc < kCols; ++cc) {
+          ak[cc] = fma2(T[cc][2 * j4 + 0], kk.x, ak[cc]);
+          aq[cc] = fma2(T[cc][2 * j4 + 0], qq.x, aq[cc]);
+          ak[cc] = fma2(T[cc][2 * j4 + 1], kk.y, ak[cc]);
+          aq[cc] = fma2(T[cc][2 * j4 + 1], qq.y, aq[cc]);
+        }
       }
-      if (TPC == 2) o += __shfl_xor_sync(0xffffffffu, o, kColsPerWarp);
-      if (half == 0) {
-        p.out_o[(row * p.Hv + h) * p.dv + col] = o;
-        p.u_out[(row * p.Hv + h) * p.dv + col] = u;
+      float4 sk, sq;
+      {
+        const float2 a0 = unpack2(ak[0]), a1 = unpack2(ak[1]), a2 = unpack2(ak[2]), a3 = unpack2(ak[3]);
+        const float2 b0 = unpack2(aq[0]), b1 = unpack2(aq[1]), b2 = unpack2(aq[2]), b3 = unpack2(aq[3]);
+        sk = make_float4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y);
+        sq = make_float4(b0.x + b0.y, b1.x + b1.y, b2.x + b2.y, b3.x + b3.y);
       }
-      if (threadIdx.x == 0 && s == 0) p.a_out[row * p.Hv + h] = a;
+      // row groups of this warp
+#pragma unroll
+      for (int m = CG; m < 32; m <<= 1) {
+        sk.x += __shfl_xor_sync(0xffffffffu, sk.x, m);
+        sk.y += __shfl_xor_sync(0xffffffffu, sk.y, m);
+        sk.z += __shfl_xor_sync(0xffffffffu, sk.z, m);
+        sk.w += __shfl_xor_sync(0xffffffffu, sk.w, m);
+        sq.x += __shfl_xor_sync(0xffffffffu, sq.x, m);
+        sq.y += __shfl_xor_sync(0xffffffffu, sq.y, m);
+        sq.z += __shfl_xor_sync(0xffffffffu, sq.z, m);
+        sq.w += __shfl_xor_sync(0xffffffffu, sq.w, m);
+      }
+      // warps: partials [parity][warp][k|q][cpb]
+      float* part = sm + L.part0() + parity * (nwarps * 2 * cpb);
+      if (lane < CG) {
+        *reinterpret_cast<float4*>(part + (warp * 2 + 0) * cpb + c0) = sk;
+        *reinterpret_cast<float4*>(part + (warp * 2 + 1) * cpb + c0) = sq;
+      }
+      __syncthreads();
+      sk = *reinterpret_cast<const float4*>(part + c0);
+#pragma unroll
+      for (int w = 1; w < nwarps; ++w) {
+        const float4 t = *reinterpret_cast<const float4*>(part + (w * 2) * cpb + c0);
+        sk.x += t.x; sk.y += t.y; sk.z += t.z; sk.w += t.w;
+      }
+      parity ^= 1;
+      const float g = sm[L.g() + node];
+      const float bt = sm[L.beta() + node];
+      const float4 v = *reinterpret_cast<const float4*>(sm + L.v(node) + c0);
+      float4 u;
+      u.x = bt * (v.x - g * sk.x);
+      u.y = bt * (v.y - g * sk.y);
+      u.z = bt * (v.z - g * sk.z);
+      u.w = bt * (v.w - g * sk.w);
+      const size_t row = nrow0 + node;
+      if (rg == 0) {
+        sq = *reinterpret_cast<const float4*>(part + cpb + c0);
+#pragma unroll
+        for (int w = 1; w < nwarps; ++w) {
+          const float4 t = *reinterpret_cast<const float4*>(part + (w * 2 + 1) * cpb + c0);
+          sq.x += t.x; sq.y += t.y; sq.z += t.z; sq.w += t.w;
+        }
+        const float kq = sm[L.kqdot() + node];
+        float4 o;
+        o.x = fmaf(u.x, kq, g * sq.x);
+        o.y = fmaf(u.y, kq, g * sq.y);
+        o.z = fmaf(u.z, kq, g * sq.z);
+        o.w = fmaf(u.w, kq, g * sq.w);
+        *reinterpret_cast<float4*>(p.out_o + (row * p.Hv + h) * p.dv + col) = o;
+        *reinterpret_cast<float4*>(p.u_out + (row * p.Hv + h) * p.dv + col) = u;
+      }
+
+      update(kvec, g, u);   // pass B
+      if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
       const int slot = bslot[node];
       if (slot >= p.nb_max) {
-        if (threadIdx.x == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+        if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
       } else if (slot >= 0) {
-        float* bs = bnd_base + static_cast<size_t>(slot) * slot_stride;
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) bs[static_cast<size_t>(r) * p.dv] = T[r];
+        store_tile(bnd_base + static_cast<size_t>(slot) * slot_stride);
       }
     }
   }
 }
 
-template <int DK, int TPC, typename InT>
+template <int DK, int RPT, int CPB, typename InT>
 cudaError_t launch_t(const VerifyParams& p, cudaStream_t s) {
-  const int cpb = min(p.dv, kVerifyThreads / TPC);    // columns per CTA
-  const int threads = cpb * TPC;
-  const size_t grid = static_cast<size_t>(p.B) * p.layers * p.Hv * (p.dv / cpb);
-  const size_t smem = p.words ? static_cast<size_t>(p.n_max) * 2 * DK * sizeof(float) : 0;
-  auto kern = chain_verify_kernel<DK, TPC, InT>;
+  constexpr int threads = (DK / RPT) * CPB / kCols;
+  static_assert(threads % 32 == 0 && threads <= kVerifyThreads, "CTA shape");
+  const size_t grid = static_cast<size_t>(p.B) * p.layers * p.Hv * (p.dv / CPB);
+  const size_t smem = smem_bytes<DK>(p.n_max, CPB, threads / 32);
+  auto kern = chain_verify_kernel<DK, RPT, CPB, InT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<static_cast<unsigned>(grid), threads, smem, s>>>(p, cpb);
+  kern<<<static_cast<unsigned>(grid), threads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+// Columns per CTA: as many as 128 threads cover, at most d_v.
+template <int DK, int RPT, typename InT>
+cudaError_t launch_dv(const VerifyParams& p, cudaStream_t s) {
+  constexpr int kMaxCols = kCols * kVerifyThreads / (DK / RPT);
+  switch (p.dv) {
+    case 32: return launch_t<DK, RPT, 32, InT>(p, s);
+    case 64: return launch_t<DK, RPT, (64 < kMaxCols ? 64 : kMaxCols), InT>(p, s);
+    case 128: return launch_t<DK, RPT, (128 < kMaxCols ? 128 : kMaxCols), InT>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <typename InT>
 cudaError_t launch_dtype(const VerifyParams& p, cudaStream_t s) {
   switch (p.dk) {
-    case 32: return launch_t<32, 1, InT>(p, s);
-    case 64: return launch_t<64, 1, InT>(p, s);
-    case 128: return launch_t<128, 2, InT>(p, s);
+    case 32: return launch_dv<32, 8, InT>(p, s);
+    case 64: return launch_dv<64, 16, InT>(p, s);
+    case 128: return launch_dv<128, 16, InT>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }
