@@ -24,6 +24,7 @@ GDN_ERR_INVALID_TREE = -2
 GDN_ERR_INVALID_PATH = -3
 GDN_ERR_UNSUPPORTED = -4
 GDN_ERR_CUDA = -5
+GDN_ERR_TIMEOUT = -6
 GDN_ERR_CAPACITY = -7
 GDN_ERR_STATE = -8
 GDN_ERR_SCHEDULE = -9

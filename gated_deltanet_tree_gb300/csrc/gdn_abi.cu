@@ -287,6 +287,9 @@ gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream) {
   if (w[0] & GDN_DEVERR_INVALID_PATH)
     return fail(GDN_ERR_INVALID_PATH, "accepted path of request %d is not a root path of its tree; nothing was "
                 "committed for it", w[1] - 1);
+  if (w[0] & GDN_DEVERR_TIMEOUT)
+    return fail(GDN_ERR_TIMEOUT, "an asynchronous copy of request %d did not complete within the bounded wait; "
+                "its outputs are incomplete", w[1] - 1);
   if (w[0] & GDN_DEVERR_SCHEDULE)
     return fail(GDN_ERR_SCHEDULE, "packed schedule of request %d is out of range (n, chains, boundary slots); "
                 "the offending accesses were skipped", w[1] - 1);

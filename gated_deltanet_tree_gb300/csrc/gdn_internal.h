@@ -88,6 +88,7 @@ struct CommitParams {
 
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+
 cudaError_t launch_commit(const CommitParams& p, int compact, cudaStream_t s);
 bool verify_supported(int dk, int dv);
 

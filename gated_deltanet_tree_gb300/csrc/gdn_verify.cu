@@ -64,6 +64,39 @@ __device__ __forceinline__ u64 mul2(u64 a, u64 b) {
   return d;
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// TMA bulk copy global -> shared completing on `bar` (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+constexpr long long kWaitCycles = 1ll << 28;   // ~0.13 s; a healthy copy completes in microseconds
+// Bounded wait for phase `parity` of `bar`; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
 template <typename InT>
 __device__ __forceinline__ float load_in(const InT* p, size_t i);
 template <>
@@ -91,6 +124,7 @@ struct Smem {
   __device__ int fg() const { return fold0() + kFoldChunk * (DK + cpb); }      // [kFoldChunk]
   __device__ int part0() const { return (fg() + kFoldChunk + 3) & ~3; }        // [2][warps][2][cpb]
   __device__ int rec0(int warps) const { return part0() + 2 * warps * 2 * cpb; } // packed schedule record
+  __device__ int bar0(int warps) const { return (rec0(warps) + SchedLayout{n_max}.words() + 3) & ~3; }  // mbarrier
 };
 
 template <int DK>
@@ -98,7 +132,8 @@ size_t smem_bytes(int n_max, int cpb, int warps) {
   const int fold0 = (n_max * (2 * DK + cpb) + 4 * n_max + 3) & ~3;
   const int part0 = (fold0 + kFoldChunk * (DK + cpb) + kFoldChunk + 3) & ~3;
   const int words = SchedLayout{n_max}.words();
-  return static_cast<size_t>(part0 + 2 * warps * 2 * cpb + words) * sizeof(float);
+  const int bar0 = (part0 + 2 * warps * 2 * cpb + words + 3) & ~3;
+  return static_cast<size_t>(bar0 + 4) * sizeof(float);
 }
 
 template <int DK, int RPT, int CPB, typename InT>
@@ -174,7 +209,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
   load_tile(st);
 
-  // ---- schedule header
+  // ---- schedule header, pending length, staging barrier
+  if (*reinterpret_cast<volatile int32_t*>(p.err) & GDN_DEVERR_TIMEOUT) return;   // an earlier CTA gave up
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar0(nwarps));
+  if (tid == 0) {
+    mbar_init(bar);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   const SchedLayout lay{p.n_max};
   const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
   int n = 0, n_chains = 0;
@@ -188,56 +230,68 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
     }
     for (int i = tid; i < lay.words(); i += blockDim.x) srec[i] = rec[i];
   }
-
-  // ---- stage the tree: k_hat, q_hat (k-head kh), v slice, gate, beta of every node
-  const InT* beta = static_cast<const InT*>(p.beta);
-  const InT* logg = static_cast<const InT*>(p.log_g);
-  const size_t nrow0 = static_cast<size_t>(bl) * p.n_max;
-  if (rec) {
-    for (int idx = tid; idx < n * (DK / 4); idx += blockDim.x) {
-      const int node = idx / (DK / 4), e4 = idx % (DK / 4);
-      const size_t src = ((nrow0 + node) * p.Hk + kh) * DK;
-      smem4[L.kq(node) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.k_in + src) + e4);
-      smem4[(L.kq(node) + DK) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.q_in + src) + e4);
-    }
-    for (int idx = tid; idx < n * (cpb / 4); idx += blockDim.x) {
-      const int node = idx / (cpb / 4), e4 = idx % (cpb / 4);
-      const size_t src = ((nrow0 + node) * p.Hv + h) * p.dv + s * cpb;
-      smem4[L.v(node) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.v_in + src) + e4);
-    }
-    for (int node = tid; node < n; node += blockDim.x) {
-      const float a = load_in<InT>(logg, (nrow0 + node) * p.Hv + h);
-      sm[L.a() + node] = a;
-      sm[L.g() + node] = expf(a);
-      sm[L.beta() + node] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
-    }
-  }
-
-  // ---- deferred commit: T <- exp(a) T + k u^T along the pending path, gathered by node index
   const int Lp = p.fold ? p.pend_len[b] : 0;
   const int32_t* path = p.pend_path + static_cast<size_t>(b) * p.n_max;
+  const size_t nrow0 = static_cast<size_t>(bl) * p.n_max;
+  __syncthreads();   // barrier initialised
+
+  // ---- asynchronous staging (TMA bulk copies): the tree's k_hat, q_hat (k-head kh) and v slice
+  // rows, and the pending path's k / u rows, chunk by chunk; gates and betas by plain loads.
+  const InT* beta = static_cast<const InT*>(p.beta);
+  const InT* logg = static_cast<const InT*>(p.log_g);
+  uint32_t phase = 0;
+  auto stage = [&](bool tree, int f0, int fn) -> bool {
+    const uint32_t bytes = (tree ? static_cast<uint32_t>(n) * (2 * DK + cpb) * 4 : 0u) +
+                           static_cast<uint32_t>(fn) * (DK + cpb) * 4;
+    if (bytes == 0) return true;
+    if (warp == 0) {
+      if (lane == 0) mbar_expect(bar, bytes);
+      __syncwarp();
+      if (tree)
+        for (int node = lane; node < n; node += 32) {
+          const size_t row = nrow0 + node;
+          bulk_g2s(sm + L.kq(node), p.k_in + (row * p.Hk + kh) * DK, DK * 4, bar);
+          bulk_g2s(sm + L.kq(node) + DK, p.q_in + (row * p.Hk + kh) * DK, DK * 4, bar);
+          bulk_g2s(sm + L.v(node), p.v_in + (row * p.Hv + h) * p.dv + s * cpb, cpb * 4, bar);
+        }
+      for (int i = lane; i < fn; i += 32) {
+        const size_t row = nrow0 + path[f0 + i];
+        bulk_g2s(sm + L.fk(i), p.pend_k + (row * p.Hk + kh) * DK, DK * 4, bar);
+        bulk_g2s(sm + L.fu(i), p.pend_u + (row * p.Hv + h) * p.dv + s * cpb, cpb * 4, bar);
+      }
+    }
+    if (tree)
+      for (int node = tid; node < n; node += blockDim.x) {
+        const float a = load_in<InT>(logg, (nrow0 + node) * p.Hv + h);
+        sm[L.a() + node] = a;
+        sm[L.g() + node] = expf(a);
+        sm[L.beta() + node] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
+      }
+    for (int i = tid; i < fn; i += blockDim.x) sm[L.fg() + i] = expf(p.pend_a[(nrow0 + path[f0 + i]) * p.Hv + h]);
+    const bool ok = mbar_wait(bar, phase);
+    phase ^= 1;
+    if (!ok) {
+      if (tid == 0) device_error(p.err, GDN_DEVERR_TIMEOUT, b);
+      mbar_wait(bar, phase ^ 1);   // let the copies land before the CTA exits
+      return false;
+    }
+    __syncthreads();   // plain-loaded scalars visible
+    return true;
+  };
+
+  // ---- deferred commit: T <- exp(a) T + k u^T along the pending path, gathered by node index
+  if (!stage(rec != nullptr, 0, min(Lp, kFoldChunk))) return;
   for (int f0 = 0; f0 < Lp; f0 += kFoldChunk) {
     const int fn = min(kFoldChunk, Lp - f0);
-    if (f0 > 0) __syncthreads();   // previous chunk consumed
-    for (int idx = tid; idx < fn * (DK / 4); idx += blockDim.x) {
-      const int i = idx / (DK / 4), e4 = idx % (DK / 4);
-      const size_t row = nrow0 + path[f0 + i];
-      smem4[L.fk(i) / 4 + e4] = __ldg(reinterpret_cast<const float4*>(p.pend_k + (row * p.Hk + kh) * DK) + e4);
+    if (f0 > 0) {
+      __syncthreads();   // previous chunk consumed
+      if (!stage(false, f0, fn)) return;
     }
-    for (int idx = tid; idx < fn * (cpb / 4); idx += blockDim.x) {
-      const int i = idx / (cpb / 4), e4 = idx % (cpb / 4);
-      const size_t row = nrow0 + path[f0 + i];
-      smem4[L.fu(i) / 4 + e4] =
-          __ldg(reinterpret_cast<const float4*>(p.pend_u + (row * p.Hv + h) * p.dv + s * cpb) + e4);
-    }
-    for (int i = tid; i < fn; i += blockDim.x) sm[L.fg() + i] = expf(p.pend_a[(nrow0 + path[f0 + i]) * p.Hv + h]);
-    __syncthreads();
     for (int i = 0; i < fn; ++i)
       update(sm + L.fk(i), sm[L.fg() + i], *reinterpret_cast<const float4*>(sm + L.fu(i) + c0));
   }
   if (Lp > 0) store_tile(st);
   if (!rec) return;  // fold only
-  __syncthreads();   // tree staging complete
 
   // ---- k . q of every node (one warp per node)
   for (int node = warp; node < n; node += blockDim.x / 32) {
