@@ -32,7 +32,8 @@ __global__ void commit_record_kernel(CommitParams p) {
   }
   int32_t* pp = p.pend_path + static_cast<size_t>(b) * p.n_max;
   if (ok) {
-    for (int i = 0; i < L; ++i) pp[i] = path[i];
+    const int32_t* heavy = rec + lay.heavy();
+    for (int i = 0; i < L; ++i) pp[i] = path[i] | ((i > 0 && heavy[path[i - 1]] != path[i]) ? kPathHeadFlag : 0);
     p.pend_len[b] = L;
   } else {
     p.pend_len[b] = 0;
@@ -47,7 +48,7 @@ __global__ void commit_record_kernel(CommitParams p) {
 __device__ __forceinline__ void compact_field(float* base, int words, const int32_t* path, int L) {
   for (int e = threadIdx.x; e < words; e += blockDim.x)
     for (int i = 0; i < L; ++i) {
-      const int src = path[i];
+      const int src = path[i] & kPathNodeMask;
       if (src != i) base[static_cast<size_t>(i) * words + e] = base[static_cast<size_t>(src) * words + e];
     }
 }
@@ -58,7 +59,7 @@ __global__ void commit_compact_kernel(CommitParams p) {
   const int L = p.pend_len[b];
   const int32_t* path = p.pend_path + static_cast<size_t>(b) * p.n_max;
   bool ident = true;
-  for (int i = 0; i < L; ++i) ident = ident && path[i] == i;
+  for (int i = 0; i < L; ++i) ident = ident && (path[i] & kPathNodeMask) == i;
   if (ident) return;
   const size_t node0 = static_cast<size_t>(bl) * p.n_max;
   switch (blockIdx.y) {
@@ -71,13 +72,13 @@ __global__ void commit_compact_kernel(CommitParams p) {
   }
 }
 
-// After compaction the recorded path is the identity.
+// After compaction the recorded path is the identity (chain-head flags kept).
 __global__ void commit_identity_kernel(CommitParams p) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.B) return;
   int32_t* pp = p.pend_path + static_cast<size_t>(b) * p.n_max;
   const int L = p.pend_len[b];
-  for (int i = 0; i < L; ++i) pp[i] = i;
+  for (int i = 0; i < L; ++i) pp[i] = i | (pp[i] & kPathHeadFlag);
 }
 
 }  // namespace

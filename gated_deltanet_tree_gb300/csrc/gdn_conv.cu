@@ -10,13 +10,17 @@
 // spanning at most 256 channels); every thread owns two adjacent channels, so
 // loads of the raw rows are 4-byte (bf16) or 8-byte (fp32) per lane and
 // coalesced.
-//   phase 1: fold the pending raw rows into the committed window (each thread
-//            owns its channels' window, so the write-back needs no barrier);
-//            for every node build the window along the parent chain, convolve,
-//            apply the activation, keep y in shared memory, copy the raw row
-//            into the factor bank;
+//   phase 0: TMA bulk copies bring the block's slice of every node's raw row
+//            into shared memory; meanwhile each thread folds the pending raw
+//            rows into its channels' committed window (it owns them, so the
+//            write-back needs no barrier) and one thread per node records the
+//            node's K-1 nearest ancestors;
+//   phase 1: for every node convolve the window (tree ancestors, then the
+//            committed rows past the root), apply SiLU, keep y in shared
+//            memory and copy the raw row into the factor bank;
 //   phase 2: one warp per (node, head): sum of squares, normalise q and k,
 //            write q_hat / k_hat / v with 16-byte stores.
+// SiLU uses the fast exp and divide intrinsics (relative error ~1e-7).
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -28,19 +32,17 @@ constexpr int kConvThreads = 128;
 constexpr int kConvChannels = 2 * kConvThreads;   // channels per CTA
 
 template <typename InT>
-struct Raw2;
+__device__ __forceinline__ float2 raw2(const InT* p);
 template <>
-struct Raw2<float> {
-  static __device__ __forceinline__ float2 load(const float* p, size_t i) {
-    return __ldg(reinterpret_cast<const float2*>(p + i));
-  }
-};
+__device__ __forceinline__ float2 raw2<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
 template <>
-struct Raw2<__nv_bfloat16> {
-  static __device__ __forceinline__ float2 load(const __nv_bfloat16* p, size_t i) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + i));
-  }
-};
+__device__ __forceinline__ float2 raw2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 
 // Head group of blockIdx.y: kind (0 q, 1 k, 2 v), first head, head count, head size.
 struct HeadGroup {
@@ -71,17 +73,58 @@ __device__ __forceinline__ HeadGroup head_group(const ConvParams& p, int y) {
 // registers); KT = 0 reads it from the parameters.
 template <typename InT, int KT>
 __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p) {
-  extern __shared__ float2 ybuf[];             // [n_max][kConvThreads] pairs of channels
+  // shared: ybuf [n_max][256] f32 | xs [n_max][256] InT | anc [n_max][K-1] int32 | mbarrier
+  extern __shared__ float4 smem_conv[];
+  float2* ybuf = reinterpret_cast<float2*>(smem_conv);
+  InT* xs = reinterpret_cast<InT*>(reinterpret_cast<char*>(smem_conv) + p.n_max * kConvChannels * 4);
+  int32_t* anc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(xs) + p.n_max * kConvChannels * sizeof(InT));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(anc + ((p.n_max * (GDN_MAX_TAPS - 1) + 3) & ~3));
   const int bl = blockIdx.x;                   // request * layers + layer
   const int b = bl / p.layers, l = bl % p.layers;
   const int tid = threadIdx.x;
   const HeadGroup hg = head_group(p, blockIdx.y);
+  const int width = hg.heads * hg.hsz;         // channels of this block
   const int c = hg.cbase + 2 * tid;            // first of this thread's two channels
-  const bool active = 2 * tid < hg.heads * hg.hsz;
+  const bool active = 2 * tid < width;
   const int K = KT > 0 ? KT : p.K, C = p.C;
   const InT* x = static_cast<const InT*>(p.x_raw);
+  if (launch_aborted(p.err)) return;
 
-  // Committed window of the two channels, oldest row first.
+  const SchedLayout lay{p.n_max};
+  const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
+  int n = 0;
+  const size_t xrow0 = static_cast<size_t>(bl) * p.n_max;   // row of node 0 of this (request, layer)
+  if (rec) {
+    n = rec[0];
+    if (n < 1 || n > p.n_max) {
+      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+      return;
+    }
+    if (tid == 0) mbar_init(bar);
+    __syncthreads();
+    if (tid < 32) {   // phase 0: raw rows of the block's channels, every node
+      if (tid == 0) mbar_expect(bar, static_cast<uint32_t>(n) * width * sizeof(InT));
+      __syncwarp();
+      for (int node = tid; node < n; node += 32)
+        bulk_g2s(xs + node * kConvChannels, x + (xrow0 + node) * C + hg.cbase, width * sizeof(InT), bar);
+    }
+    const int32_t* parent = rec + lay.parent();
+    for (int node = tid; node < n; node += kConvThreads) {
+      // ancestors 1..K-1 along the root path; -(j+1) = committed row K-1-j when the path runs out
+      int m = parent[node], back = 0;
+      for (int i = 1; i < K; ++i) {
+        if (m >= 0 && m < node) {
+          anc[node * (GDN_MAX_TAPS - 1) + i - 1] = m;
+          m = parent[m];
+        } else {
+          anc[node * (GDN_MAX_TAPS - 1) + i - 1] = -(++back);
+          m = -1;
+        }
+      }
+    }
+  }
+
+  // Committed window of the two channels, oldest row first (fold the pending rows in first).
   float2 win[GDN_MAX_TAPS - 1];
   if (p.conv_mode == 1 && active) {
     float* cs = p.conv_state + static_cast<size_t>(bl) * (K - 1) * C + c;
@@ -95,24 +138,15 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p)
         for (int i = (L > K - 1 ? L - (K - 1) : 0); i < L; ++i) {
 #pragma unroll
           for (int j = 0; j + 1 < K - 1; ++j) win[j] = win[j + 1];
-          if (K > 1) win[K - 2] = *reinterpret_cast<const float2*>(px + static_cast<size_t>(path[i]) * C);
+          if (K > 1)
+            win[K - 2] = *reinterpret_cast<const float2*>(px + static_cast<size_t>(path[i] & kPathNodeMask) * C);
         }
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) *reinterpret_cast<float2*>(cs + static_cast<size_t>(j) * C) = win[j];
       }
     }
   }
-  if (p.words == nullptr) return;  // fold only
-
-  const SchedLayout lay{p.n_max};
-  const int32_t* rec = p.words + static_cast<size_t>(b) * lay.words();
-  const int n = rec[0];
-  if (n < 1 || n > p.n_max) {
-    if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-    return;
-  }
-  const int32_t* parent = rec + lay.parent();
-  const size_t xrow0 = static_cast<size_t>(bl) * p.n_max;   // row of node 0 of this (request, layer)
+  if (rec == nullptr) return;  // fold only
 
   float2 w[GDN_MAX_TAPS];
   if (p.conv_mode == 1 && active) {
@@ -120,43 +154,46 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p)
 #pragma unroll
     for (int j = 0; j < K; ++j) w[j] = make_float2(cw[j], cw[K + j]);
   }
+  if (!mbar_wait(bar, 0)) {
+    if (tid == 0) device_error(p.err, GDN_DEVERR_TIMEOUT, b);
+    mbar_wait(bar, 0);
+    return;
+  }
+  __syncthreads();   // ancestor table visible
 
   // phase 1: conv + activation of every node
   for (int node = 0; node < n; ++node) {
     float2 y = make_float2(0.f, 0.f);
     if (active) {
-      const float2 xs = Raw2<InT>::load(x, (xrow0 + node) * C + c);
-      y = xs;
+      const float2 xs0 = raw2<InT>(xs + node * kConvChannels + 2 * tid);
+      y = xs0;
       if (p.conv_mode == 1) {
         // tap K-1 multiplies the node itself, tap K-1-i its i-th predecessor on the
         // root path; past the root the committed window supplies the rows.
-        y.x = w[K - 1].x * xs.x;
-        y.y = w[K - 1].y * xs.y;
-        int m = parent[node];
-        int ci = K - 2;
+        y.x = w[K - 1].x * xs0.x;
+        y.y = w[K - 1].y * xs0.y;
 #pragma unroll
         for (int i = 1; i < K; ++i) {
+          const int a = anc[node * (GDN_MAX_TAPS - 1) + i - 1];
           float2 xv;
-          if (m >= 0 && m < node) {
-            xv = Raw2<InT>::load(x, (xrow0 + m) * C + c);
-            m = parent[m];
+          if (a >= 0) {
+            xv = raw2<InT>(xs + a * kConvChannels + 2 * tid);
           } else {
-            // win[ci] with a register-resident window: select instead of a dynamic index
+            // committed row K-1+a (a = -1 is the latest); register-resident select
+            const int ci = K - 1 + a;
             xv = win[0];
 #pragma unroll
             for (int j = 1; j < GDN_MAX_TAPS - 1; ++j)
               if (j < K - 1 && j == ci) xv = win[j];
-            --ci;
-            m = -1;
           }
           y.x = fmaf(w[K - 1 - i].x, xv.x, y.x);
           y.y = fmaf(w[K - 1 - i].y, xv.y, y.y);
         }
-        *reinterpret_cast<float2*>(p.x_out + (xrow0 + node) * C + c) = xs;
+        *reinterpret_cast<float2*>(p.x_out + (xrow0 + node) * C + c) = xs0;
       }
       if (p.act == 1) {
-        y.x = y.x / (1.f + expf(-y.x));
-        y.y = y.y / (1.f + expf(-y.y));
+        y.x = silu(y.x);
+        y.y = silu(y.y);
       }
     }
     ybuf[node * kConvThreads + tid] = y;
@@ -194,7 +231,10 @@ template <typename InT, int KT>
 cudaError_t launch_t(const ConvParams& p, cudaStream_t s) {
   const int hq = kConvChannels / p.dk, hv = kConvChannels / p.dv;
   dim3 grid(p.B * p.layers, 2 * ((p.Hk + hq - 1) / hq) + (p.Hv + hv - 1) / hv);
-  const size_t smem = p.words ? static_cast<size_t>(p.n_max) * kConvThreads * sizeof(float2) : 0;
+  const size_t smem =
+      p.words ? static_cast<size_t>(p.n_max) * kConvChannels * (4 + sizeof(InT)) +
+                    ((p.n_max * (GDN_MAX_TAPS - 1) + 3) & ~3) * 4 + 16
+              : 0;
   auto k = conv_window_kernel<InT, KT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

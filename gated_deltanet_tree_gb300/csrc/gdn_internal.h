@@ -18,18 +18,65 @@ __device__ __forceinline__ void device_error(int32_t* err, int bit, int b) {
   atomicOr(&err[0], bit);
   atomicCAS(&err[1], 0, b + 1);
 }
+
+// ---- TMA bulk copies completing on an mbarrier (shared by the kernels) ----
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// Global -> shared bulk copy completing on `bar` (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+constexpr long long kWaitCycles = 1ll << 28;   // ~0.13 s; a healthy copy completes in microseconds
+// Bounded wait for phase `parity` of `bar`; false on timeout (the caller flags GDN_DEVERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+// True once some CTA of this launch gave up on a wait: later CTAs exit at once.
+__device__ __forceinline__ bool launch_aborted(const int32_t* err) {
+  return (*reinterpret_cast<const volatile int32_t*>(err) & GDN_DEVERR_TIMEOUT) != 0;
+}
 #endif
 
 // Offsets inside one packed schedule record (see gdn_tree.h).
 struct SchedLayout {
   int n_max;
-  __host__ __device__ int words() const { return 5 + 5 * n_max; }
+  __host__ __device__ int words() const { return 5 + 6 * n_max; }
   __host__ __device__ int parent() const { return 4; }
   __host__ __device__ int bslot() const { return 4 + n_max; }
   __host__ __device__ int chain_src() const { return 4 + 2 * n_max; }
   __host__ __device__ int chain_off() const { return 4 + 3 * n_max; }
   __host__ __device__ int chain_nodes() const { return 5 + 4 * n_max; }
+  __host__ __device__ int heavy() const { return 5 + 5 * n_max; }
 };
+
+// Encoding of a recorded pending-path entry: node index in the low bits; the
+// head flag marks a node that starts a new chain (its parent's light child),
+// where the verify materialised the state and reloaded it.
+constexpr int32_t kPathNodeMask = 0xFFFF;
+constexpr int32_t kPathHeadFlag = 1 << 30;
 
 struct ConvParams {
   int B, layers, n_max;

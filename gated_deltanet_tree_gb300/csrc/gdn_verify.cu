@@ -28,8 +28,19 @@
 // shared memory once per tree, and the pending path's factors once per chunk of
 // the fold, so the node loop issues no global loads.
 //
-// The fold applies the same pass B with the same u, so the committed state
-// reproduces, bit for bit, the state the earlier verify computed at that node.
+// Lazy decay: a chain keeps its tile as T~ with a scalar gamma, the state being
+// gamma * T~.  A node multiplies only the scalar (gamma' = gamma g), so pass B
+// is one FMA per element, T~ += k (u / gamma')^T, and pass A reads
+// p = gamma' T~^T k, o = gamma' T~^T q + u (k . q).  The tile is materialised
+// (T~ <- gamma T~, gamma = 1) only where the state leaves the registers -- at
+// boundary slots and the committed write -- and when gamma' falls below
+// kGammaFloor (which also covers g = 0), where that node applies its decay to
+// the tile before the update.
+//
+// The fold repeats exactly these operations with the same u -- including the
+// materialisation wherever the accepted path enters a light child, where the
+// verify reloaded the stored state -- so the committed state reproduces, bit
+// for bit, the state the earlier verify stored for that node.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -40,6 +51,7 @@ namespace {
 constexpr int kVerifyThreads = 128;
 constexpr int kCols = 4;           // columns per thread
 constexpr int kFoldChunk = 16;     // pending nodes staged per fold step
+constexpr float kGammaFloor = 1.0e-12f;   // below this the decay is applied to the tile at once
 
 typedef unsigned long long u64;
 
@@ -62,39 +74,6 @@ __device__ __forceinline__ u64 mul2(u64 a, u64 b) {
   u64 d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-// TMA bulk copy global -> shared completing on `bar` (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-constexpr long long kWaitCycles = 1ll << 28;   // ~0.13 s; a healthy copy completes in microseconds
-// Bounded wait for phase `parity` of `bar`; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
 }
 
 template <typename InT>
@@ -190,7 +169,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
           make_float4(a0.y, a1.y, a2.y, a3.y);
     }
   };
-  // pass B on every column: T <- fmaf(k, u_c, g * T)
+  // pass B with the decay: T <- fmaf(k, u_c, g * T)
   auto update = [&](const float* kvec, float g, float4 u) {
     const u64 g2 = pack2(g, g);
     const u64 u2[kCols] = {pack2(u.x, u.x), pack2(u.y, u.y), pack2(u.z, u.z), pack2(u.w, u.w)};
@@ -205,18 +184,60 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       }
     }
   };
+  // pass B without the decay: T~ <- fmaf(k, ut_c, T~)
+  auto update_lazy = [&](const float* kvec, float4 ut) {
+    const u64 u2[kCols] = {pack2(ut.x, ut.x), pack2(ut.y, ut.y), pack2(ut.z, ut.z), pack2(ut.w, ut.w)};
+    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
+#pragma unroll
+    for (int j4 = 0; j4 < NP / 2; ++j4) {
+      const ulonglong2 kk = k4[j4];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        T[c][2 * j4 + 0] = fma2(kk.x, u2[c], T[c][2 * j4 + 0]);
+        T[c][2 * j4 + 1] = fma2(kk.y, u2[c], T[c][2 * j4 + 1]);
+      }
+    }
+  };
+  // T~ <- gamma T~
+  auto materialise = [&](float gam) {
+    const u64 g2 = pack2(gam, gam);
+#pragma unroll
+    for (int c = 0; c < kCols; ++c)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) T[c][j] = mul2(g2, T[c][j]);
+  };
+  // one node of the gated delta rule on the lazy tile; returns the new gamma.  Below the
+  // floor the decay goes into the tile first (the same mul-then-fma rounding as a direct
+  // decayed update), then the update is the plain one.
+  auto advance = [&](const float* kvec, float gam1, float4 u) -> float {
+    if (gam1 < kGammaFloor) {
+      materialise(gam1);
+      gam1 = 1.f;
+    }
+    const float r = __frcp_rn(gam1);
+    update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
+    return gam1;
+  };
+  // store gamma T~ without touching the registers
+  auto store_scaled = [&](float* base, float gam) {
+    const u64 g2 = pack2(gam, gam);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      const float2 a0 = unpack2(mul2(g2, T[0][j])), a1 = unpack2(mul2(g2, T[1][j]));
+      const float2 a2 = unpack2(mul2(g2, T[2][j])), a3 = unpack2(mul2(g2, T[3][j]));
+      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j) * p.dv) = make_float4(a0.x, a1.x, a2.x, a3.x);
+      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv) =
+          make_float4(a0.y, a1.y, a2.y, a3.y);
+    }
+  };
 
   float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
   load_tile(st);
 
   // ---- schedule header, pending length, staging barrier
-  if (*reinterpret_cast<volatile int32_t*>(p.err) & GDN_DEVERR_TIMEOUT) return;   // an earlier CTA gave up
+  if (launch_aborted(p.err)) return;   // an earlier CTA gave up on a wait
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar0(nwarps));
-  if (tid == 0) {
-    mbar_init(bar);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
+  if (tid == 0) mbar_init(bar);
   const SchedLayout lay{p.n_max};
   const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
   int n = 0, n_chains = 0;
@@ -255,7 +276,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
           bulk_g2s(sm + L.v(node), p.v_in + (row * p.Hv + h) * p.dv + s * cpb, cpb * 4, bar);
         }
       for (int i = lane; i < fn; i += 32) {
-        const size_t row = nrow0 + path[f0 + i];
+        const size_t row = nrow0 + (path[f0 + i] & kPathNodeMask);
         bulk_g2s(sm + L.fk(i), p.pend_k + (row * p.Hk + kh) * DK, DK * 4, bar);
         bulk_g2s(sm + L.fu(i), p.pend_u + (row * p.Hv + h) * p.dv + s * cpb, cpb * 4, bar);
       }
@@ -267,7 +288,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         sm[L.g() + node] = expf(a);
         sm[L.beta() + node] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
       }
-    for (int i = tid; i < fn; i += blockDim.x) sm[L.fg() + i] = expf(p.pend_a[(nrow0 + path[f0 + i]) * p.Hv + h]);
+    for (int i = tid; i < fn; i += blockDim.x)
+      sm[L.fg() + i] = expf(p.pend_a[(nrow0 + (path[f0 + i] & kPathNodeMask)) * p.Hv + h]);
     const bool ok = mbar_wait(bar, phase);
     phase ^= 1;
     if (!ok) {
@@ -280,6 +302,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   };
 
   // ---- deferred commit: T <- exp(a) T + k u^T along the pending path, gathered by node index
+  float gam = 1.f;               // the state is gam * T
   if (!stage(rec != nullptr, 0, min(Lp, kFoldChunk))) return;
   for (int f0 = 0; f0 < Lp; f0 += kFoldChunk) {
     const int fn = min(kFoldChunk, Lp - f0);
@@ -287,10 +310,19 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       __syncthreads();   // previous chunk consumed
       if (!stage(false, f0, fn)) return;
     }
-    for (int i = 0; i < fn; ++i)
-      update(sm + L.fk(i), sm[L.fg() + i], *reinterpret_cast<const float4*>(sm + L.fu(i) + c0));
+    for (int i = 0; i < fn; ++i) {
+      if (path[f0 + i] & kPathHeadFlag) {   // the verify stored and reloaded the state here
+        materialise(gam);
+        gam = 1.f;
+      }
+      gam = advance(sm + L.fk(i), gam * sm[L.fg() + i], *reinterpret_cast<const float4*>(sm + L.fu(i) + c0));
+    }
   }
-  if (Lp > 0) store_tile(st);
+  if (Lp > 0) {
+    materialise(gam);            // the committed state; verification continues from exactly these values
+    gam = 1.f;
+    store_tile(st);
+  }
   if (!rec) return;  // fold only
 
   // ---- k . q of every node (one warp per node)
@@ -321,7 +353,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
       return;
     }
-    if (src >= 0) load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
+    if (src >= 0) {
+      load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
+      gam = 1.f;
+    }
     for (int i = i0; i < i1; ++i) {
       const int node = cnodes[i];
       if (node < 0 || node >= n) {
@@ -381,7 +416,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         sk.x += t.x; sk.y += t.y; sk.z += t.z; sk.w += t.w;
       }
       parity ^= 1;
-      const float g = sm[L.g() + node];
+      const float g = gam * sm[L.g() + node];   // gamma' of this node
       const float bt = sm[L.beta() + node];
       const float4 v = *reinterpret_cast<const float4*>(sm + L.v(node) + c0);
       float4 u;
@@ -407,13 +442,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         *reinterpret_cast<float4*>(p.u_out + (row * p.Hv + h) * p.dv + col) = u;
       }
 
-      update(kvec, g, u);   // pass B
+      gam = advance(kvec, g, u);   // pass B
       if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
       const int slot = bslot[node];
       if (slot >= p.nb_max) {
         if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
       } else if (slot >= 0) {
-        store_tile(bnd_base + static_cast<size_t>(slot) * slot_stride);
+        store_scaled(bnd_base + static_cast<size_t>(slot) * slot_stride, gam);
       }
     }
   }

@@ -167,6 +167,7 @@ extern "C" gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* 
       w[lay.parent() + i] = parents[static_cast<size_t>(b) * n_max + i];
       w[lay.bslot() + i] = h.bslot[i];
       w[lay.chain_nodes() + i] = h.chain_nodes[i];
+      w[lay.heavy() + i] = h.heavy[i];
     }
     for (int c = 0; c < h.n_chains; ++c) w[lay.chain_src() + c] = h.chain_src[c];
     for (int c = 0; c <= h.n_chains; ++c) w[lay.chain_off() + c] = h.chain_off[c];

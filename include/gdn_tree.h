@@ -120,6 +120,7 @@ gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_schedule* out)
  *   [4+2n_max .. 4+3n_max)      source slot of each chain in schedule order
  *   [4+3n_max .. 5+4n_max)      chain offsets into the node list
  *   [5+4n_max .. 5+5n_max)      nodes of the chains, concatenated
+ *   [5+5n_max .. 5+6n_max)      heavy child of each node (-1: leaf)
  * gdn_pack_schedules runs gdn_hld_schedule on every request's tree and writes
  * the records into words_host (B * gdn_schedule_words(n_max) int32, caller-
  * owned host memory); *nb_max_out receives the largest boundary count.  The
@@ -149,7 +150,9 @@ typedef struct {
  *   a[i] [B][layers][n_max][Hv]        x[i] [B][layers][n_max][C]  (C = 2 Hk dk + Hv dv;
  *                                           only read/written in conv_mode 1, may be NULL otherwise)
  *   pend_path [B][n_max] int32, pend_len [B] int32: the accepted path recorded by
- *   gdn_commit_fold; err [4] int32, zeroed by the caller before first use.
+ *   gdn_commit_fold -- node index in the low 16 bits, bit 30 set where the path
+ *   enters a light child (a chain head); err [4] int32, zeroed by the caller
+ *   before first use.
  * Host fields (set by gdn_banks_init, then advanced by the calls):
  *   write_bank: bank the next verify writes; pend_bank: bank holding the
  *   committed-but-not-folded path (-1: none); verified_bank: bank written by

@@ -83,7 +83,7 @@ def test_packed_layout(N):
     for b, t in enumerate(trees):
         P[b, :len(t)] = t
     words, nb_max = N.gdn_pack_schedules(P, n)
-    assert words.shape == (len(trees), 5 + 5 * n_max)
+    assert words.shape == (len(trees), 5 + 6 * n_max)
     assert nb_max == max(O.hld_schedule(list(t))["n_boundary"] for t in trees)
     for b, t in enumerate(trees):
         s = O.hld_schedule(list(t))
@@ -96,6 +96,7 @@ def test_packed_layout(N):
         assert list(w[4 + 2 * n_max:4 + 2 * n_max + nc]) == s["chain_src_slot"]
         assert list(w[4 + 3 * n_max:5 + 3 * n_max + nc]) == s["chain_off"]
         assert list(w[5 + 4 * n_max:5 + 4 * n_max + m]) == s["chain_nodes"]
+        assert list(w[5 + 5 * n_max:5 + 5 * n_max + m]) == s["heavy"]
     with pytest.raises(N.GdnError) as e:
         N.gdn_pack_schedules(np.full((1, 65), -1, dtype=np.int32), np.array([3], dtype=np.int32))
     assert e.value.status == N.GDN_ERR_UNSUPPORTED
