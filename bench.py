@@ -163,32 +163,66 @@ def _warm_worker(_):
     return 0
 
 
-def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None):
-    """Oracle verify (one full root-path replay per node) on a sample of (request, layer) blocks."""
+def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None, warmup: int = 0, steps: int = 0):
+    """Oracle verify (one full root-path replay per node) on a sample of (request, layer) blocks.
+
+    With steps > 0: `warmup` untimed and `steps` timed steps, each one block per host process.
+    Otherwise: as many such steps as fit in about `target_s` seconds.
+    """
     import dataclasses
     cores = cores or os.cpu_count() or 1
     kw = dataclasses.asdict(w)
     units = [(kw, b, l) for l in range(w.layers) for b in range(w.B)]
-    rng = np.random.default_rng(0)
-    order = rng.permutation(len(units))
+    order = np.random.default_rng(0).permutation(len(units))
     ctx = mp.get_context("spawn")
-    done_units, blocks = 0, 0
+    done_units, blocks, pos, timed_steps = 0, 0, 0, 0
+
+    def next_batch():
+        nonlocal pos
+        batch = [units[order[(pos + i) % len(units)]] for i in range(cores)]
+        pos += cores
+        return batch
+
     with ctx.Pool(cores) as pool:
         pool.map(_warm_worker, range(cores))      # spawn and imports are not timed
+        for _ in range(warmup):
+            pool.map(_oracle_unit, next_batch())
         t0 = time.perf_counter()
-        pos = 0
-        while pos < len(order):
-            batch = [units[i] for i in order[pos:pos + cores]]
-            pos += len(batch)
-            for u, _ in pool.map(_oracle_unit, batch):
+        while True:
+            for u, _ in pool.map(_oracle_unit, next_batch()):
                 done_units += u
                 blocks += 1
-            if time.perf_counter() - t0 >= target_s:
+            timed_steps += 1
+            if steps > 0 and timed_steps >= steps:
+                break
+            if steps <= 0 and time.perf_counter() - t0 >= target_s:
                 break
     dt = time.perf_counter() - t0
-    return {"value": done_units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{blocks} of {w.B * w.layers} (request, layer) blocks of step 0, all {w.Hv} v-heads and "
-                      f"every node, {dt:.1f} s wall on {cores} host processes (spawn pool)"}
+    return {"value": done_units / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "steps": timed_steps,
+            "ms_per_step": dt * 1e3 / timed_steps,
+            "sample": f"{blocks} of {w.B * w.layers} (request, layer) blocks of step 0 ({timed_steps} steps of "
+                      f"{cores}), all {w.Hv} v-heads and every node, {dt:.1f} s wall on {cores} host processes "
+                      f"(spawn pool)"}
+
+
+def reduce_across_ranks(ms: float, units: float, e2e_ms: float, e2e_units: float, device=None):
+    """Whole-job figures: the slowest rank's time, the units of all ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, units, e2e_ms, e2e_units
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([units, e2e_units], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(u[0]), float(t[1]), float(u[1])
+
+
+def rank_plan_trees(w: S.Workload, rank: int):
+    """Every rank serves its own requests: request ids are offset by rank * B."""
+    trees = [[S.tree_for(w, b + rank * w.B, s) for b in range(w.B)] for s in range(w.steps)]
+    paths = [[S.path_for(w, trees[s][b], b + rank * w.B, s) for b in range(w.B)] for s in range(w.steps)]
+    return trees, paths
 
 
 # ----------------------------------------------------------------------------
@@ -205,10 +239,8 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     # every rank serves its own requests: request ids are offset by rank
-    plan_w = w
-    plan = WorkloadPlan(plan_w, trees=[[S.tree_for(w, b + rank * w.B, s) for b in range(w.B)]
-                                       for s in range(w.steps)])
-    plan.paths = [[S.path_for(w, plan.trees[s][b], b + rank * w.B, s) for b in range(w.B)] for s in range(w.steps)]
+    trees, paths_h = rank_plan_trees(w, rank)
+    plan = WorkloadPlan(w, trees=trees, paths=paths_h)
     gs = GpuSession(w, plan, device=dev, preload_steps=range(w.steps))
     stream = torch.cuda.current_stream(dev)
     ver = gs.ver
@@ -302,16 +334,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         e2e = run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct,
                       units_per_step)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e["ms"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
-        u = torch.tensor([timed_units, e2e["units"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(u, op=dist.ReduceOp.SUM)
-        timed_units_all, e2e_units_all = float(u[0]), float(u[1])
-    else:
-        e2e_ms = e2e["ms"]
-        timed_units_all, e2e_units_all = timed_units, e2e["units"]
+    ms, timed_units_all, e2e_ms, e2e_units_all = reduce_across_ranks(ms, timed_units, e2e["ms"], e2e["units"], dev)
 
     peak, peak_kind = peaks()
     avg_verify_s = statistics.mean(verify_ms) / 1e3
@@ -392,9 +415,10 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        base = oracle_throughput(w, target_s=max(10.0, min(60.0, 4.0 * args.steps)))
+        base = oracle_throughput(w, warmup=args.warmup, steps=args.steps)
         line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": base["ms_per_step"],
+                "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": base,
                 "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

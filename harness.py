@@ -50,22 +50,24 @@ class GpuSession:
     """Device state of a workload: recurrent state, conv window, per-step inputs, outputs."""
 
     def __init__(self, w: S.Workload, plan: Optional[WorkloadPlan] = None, device="cuda",
-                 preload_steps: Sequence[int] = ()):
+                 preload_steps: Sequence[int] = (), layer_ids: Optional[Sequence[int]] = None):
         self.w = w
         self.plan = plan or WorkloadPlan(w)
         self.device = torch.device(device)
         self.dims = dims_for(w)
         self.bf16 = w.in_dtype == S.DTYPE_BF16
-        self.ver = TreeVerifier(self.dims, w.B, w.layers, w.n_max, device)
+        # the call covers these layers of the workload (all by default; a subset for layer-chunked calls)
+        self.layer_ids = list(range(w.layers)) if layer_ids is None else list(layer_ids)
+        B, L, n = w.B, len(self.layer_ids), w.n_max
+        self.ver = TreeVerifier(self.dims, B, L, n, device)
         f32 = dict(dtype=torch.float32, device=self.device)
-        B, L, n = w.B, w.layers, w.n_max
         self.state = torch.empty(B, L, w.Hv, w.dk, w.dv, **f32)
         self.conv_state = torch.empty(B, L, max(w.K - 1, 0), w.C, **f32)
         for b in range(B):
-            T, W = S.batch_state(w, requests=[b])
+            T, W = S.batch_state(w, requests=[b], layers=self.layer_ids)
             self.state[b].copy_(torch.from_numpy(T[0]))
             self.conv_state[b].copy_(torch.from_numpy(W[0]))
-        self.conv_w = torch.from_numpy(S.batch_conv_weight(w)).to(self.device)
+        self.conv_w = torch.from_numpy(S.batch_conv_weight(w, layers=self.layer_ids)).to(self.device)
         self.out_o = torch.zeros(B, L, n, w.Hv, w.dv, **f32)
         self.nb_cap = max(self.plan.nb_cap, 1)
         self.boundary = torch.zeros(B, L, self.nb_cap, w.Hv, w.dk, w.dv, **f32)
@@ -78,11 +80,12 @@ class GpuSession:
     def _upload_step(self, step: int):
         w = self.w
         in_dt = torch.bfloat16 if self.bf16 else torch.float32
-        X = torch.empty(w.B, w.layers, w.n_max, w.C, dtype=in_dt, device=self.device)
-        BE = torch.empty(w.B, w.layers, w.n_max, w.Hv, dtype=in_dt, device=self.device)
-        AG = torch.empty(w.B, w.layers, w.n_max, w.Hv, dtype=in_dt, device=self.device)
+        L = len(self.layer_ids)
+        X = torch.empty(w.B, L, w.n_max, w.C, dtype=in_dt, device=self.device)
+        BE = torch.empty(w.B, L, w.n_max, w.Hv, dtype=in_dt, device=self.device)
+        AG = torch.empty(w.B, L, w.n_max, w.Hv, dtype=in_dt, device=self.device)
         for b in range(w.B):
-            x, be, ag = S.batch_node_inputs(w, step, requests=[b])
+            x, be, ag = S.batch_node_inputs(w, step, requests=[b], layers=self.layer_ids)
             X[b].copy_(host_to_device(x[0], "cpu", self.bf16))
             BE[b].copy_(host_to_device(be[0], "cpu", self.bf16))
             AG[b].copy_(host_to_device(ag[0], "cpu", self.bf16))
@@ -107,6 +110,9 @@ class GpuSession:
         X, BE, AG = self.step_inputs(step)
         self.ver.verify(self.schedule(step), X, self.conv_w, BE, AG, self.state, self.conv_state, self.out_o,
                         self.boundary, stream)
+
+    def local_layer(self, l: int) -> int:
+        return self.layer_ids.index(l)
 
     def commit(self, step: int, compact: bool = False, stream=None):
         P, L = self.paths(step)

@@ -27,20 +27,24 @@ def _np(t):
     return t.detach().cpu().numpy().astype(np.float64)
 
 
-def run_parity(w, units=None, compact_steps=(), finish=True, plan=None):
-    """Run every step of workload w on the GPU; compare the chosen units with the oracle."""
+def run_parity(w, units=None, compact_steps=(), finish=True, plan=None, layer_ids=None):
+    """Run every step of workload w on the GPU; compare the chosen units with the oracle.
+
+    layer_ids: the layers one call covers (a layer chunk); units must lie in it.
+    """
     from harness import GpuSession, WorkloadPlan
     plan = plan or WorkloadPlan(w)
-    gs = GpuSession(w, plan)
+    gs = GpuSession(w, plan, layer_ids=layer_ids)
     if units is None:
-        units = [(b, l) for b in range(w.B) for l in range(w.layers)]
+        units = [(b, l) for b in range(w.B) for l in gs.layer_ids]
     oracles = {u: OracleUnit(w, plan, *u) for u in units}
     worst = dict(o=0.0, state=0.0, boundary=0.0)
     for s in range(w.steps):
         gs.verify(s)
         bank = gs.ver.banks.verified_bank
         torch.cuda.synchronize()
-        for (b, l), ou in oracles.items():
+        for (b, lg), ou in oracles.items():
+            l = gs.local_layer(lg)
             exp = ou.verify(s)
             n = exp["n"]
             worst["o"] = max(worst["o"], check_o(_np(gs.out_o[b, l, :n]), exp["o"], f"o step {s} unit {(b, l)}"))
@@ -69,10 +73,12 @@ def run_parity(w, units=None, compact_steps=(), finish=True, plan=None):
                     assert torch.equal(post[:, len(path):], t[b][:, len(path):]), f
         for ou in oracles.values():
             ou.commit(s)
+        gs.drop_step(s)
     if finish:
         gs.finish()
         torch.cuda.synchronize()
-        for (b, l), ou in oracles.items():
+        for (b, lg), ou in oracles.items():
+            l = gs.local_layer(lg)
             T, W = ou.committed()
             check_state(_np(gs.state[b, l]), T, f"state after finish unit {(b, l)}")
             if w.conv_mode == 1 and w.K > 1:
@@ -152,6 +158,53 @@ def test_qwen_48_layers_commit_then_verify():
 def test_batched_32x48_eight_steps():
     w = S.workload(4)
     run_parity(w, units=[(0, 0), (13, 29), (31, 47)])
+
+
+@pytest.mark.parametrize("cfg", [5, 6], ids=["ddtree64_top8", "chain64"])
+def test_stress_128_requests_layer_chunked(cfg):
+    # 128 requests x 48 layers of 64-node trees: the boundary states alone would take ~360 GB,
+    # so calls cover 8 layers at a time; the chunks holding the sampled units run all steps
+    w = S.workload(cfg).replace(steps=3)
+    from harness import WorkloadPlan
+    plan = WorkloadPlan(w)
+    for layers, units in ((range(0, 8), [(0, 0), (127, 5)]), (range(40, 48), [(77, 41), (3, 47)])):
+        run_parity(w, units=units, plan=plan, layer_ids=layers)
+
+
+def test_checkpoint_resume_is_bitwise():
+    """finish -> save {state, conv window} -> fresh session -> continue equals the uninterrupted run."""
+    import io
+    from harness import GpuSession, WorkloadPlan
+    w = S.workload(2).replace(B=2, layers=2, steps=4)
+    plan = WorkloadPlan(w)
+    ref = GpuSession(w, plan)
+    outs = {}
+    for s in range(w.steps):
+        ref.verify(s)
+        outs[s] = ref.out_o.clone()
+        ref.commit(s)
+    ref.finish()
+    a = GpuSession(w, plan)
+    for s in range(2):
+        a.verify(s)
+        a.commit(s)
+    a.finish()
+    buf = io.BytesIO()
+    torch.save({"state": a.state.cpu(), "conv_state": a.conv_state.cpu()}, buf)
+    buf.seek(0)
+    ck = torch.load(buf)
+    b = GpuSession(w, plan)
+    b.state.copy_(ck["state"])
+    b.conv_state.copy_(ck["conv_state"])
+    for s in range(2, w.steps):
+        b.verify(s)
+        torch.cuda.synchronize()
+        assert torch.equal(b.out_o, outs[s]), s
+        b.commit(s)
+    b.finish()
+    torch.cuda.synchronize()
+    assert torch.equal(b.state, ref.state)
+    assert torch.equal(b.conv_state, ref.conv_state)
 
 
 # ---------------------------------------------------------------------------
