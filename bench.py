@@ -347,6 +347,9 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
 
 
 def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct, units_per_step):
+    """Same calls with host buffers: each step copies its inputs from pinned host memory and reads its
+    outputs back.  Copies run on their own streams, double-buffered, so step k+1's upload and step k-1's
+    download overlap step k's compute; the timed span runs from the first upload to the last download."""
     import torch
     from gated_deltanet_tree_gb300 import _native as N
     steps = max(1, min(args.steps, 8))
@@ -355,30 +358,53 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
     for s in range(nsrc):
         X, BE, AG = gs.inputs[s]
         host_in.append(tuple(t.cpu().pin_memory() for t in (X, BE, AG)))
-    o_host = torch.empty(gs.out_o.shape, dtype=gs.out_o.dtype).pin_memory()
-    X_d, BE_d, AG_d = (torch.empty_like(t) for t in gs.inputs[0])
-    h2d = sum(t.numel() * t.element_size() for t in host_in[0]) + words_host[0].numel() * 4
-    d2h = o_host.numel() * o_host.element_size()
+    dev_in = [tuple(torch.empty_like(t) for t in gs.inputs[0]) for _ in range(2)]
+    out = [gs.out_o, torch.empty_like(gs.out_o)]
+    o_host = [torch.empty(gs.out_o.shape, dtype=gs.out_o.dtype).pin_memory() for _ in range(2)]
+    wh = [torch.empty_like(words_host[0]).pin_memory() for _ in range(steps)]
+    wd = [torch.empty_like(words_dev[0]) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0]) + wh[0].numel() * 4
+    d2h = o_host[0].numel() * o_host[0].element_size()
     ver = gs.ver
+    # three streams of their own: the default stream would serialise with the copy streams
+    stream = torch.cuda.Stream(dev)
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    h2d_done = [ev() for _ in range(steps)]
+    cmp_done = [ev() for _ in range(steps)]
+    d2h_done = [ev() for _ in range(steps)]
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     units = 0
-    e0.record(stream)
+    e0.record(s_h2d)
     for k in range(steps):
-        s = k % nsrc
+        i, s = k % 2, k % nsrc
         P, n = parents_host[s]
-        words, _ = N.gdn_pack_schedules(P, n)
-        words_host[s].numpy()[...] = words
-        words_dev[s].copy_(words_host[s], non_blocking=True)
-        for dst, src in zip((X_d, BE_d, AG_d), host_in[s]):
-            dst.copy_(src, non_blocking=True)
-        sc = sched_struct(s)
-        N.gdn_tree_verify(gs.dims, w.layers, sc, X_d, gs.conv_w, BE_d, AG_d, gs.state, gs.conv_state, gs.out_o,
+        words, _ = N.gdn_pack_schedules(P, n)            # host heavy-light schedules
+        wh[k].numpy()[...] = words
+        with torch.cuda.stream(s_h2d):
+            if k >= 2:
+                s_h2d.wait_event(cmp_done[k - 2])        # buffers i no longer read by compute
+            wd[i].copy_(wh[k], non_blocking=True)
+            for dst, src in zip(dev_in[i], host_in[s]):
+                dst.copy_(src, non_blocking=True)
+            h2d_done[k].record(s_h2d)
+        stream.wait_event(h2d_done[k])
+        if k >= 2:
+            stream.wait_event(d2h_done[k - 2])           # output buffer i downloaded
+        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, words=wd[i].data_ptr())
+        X_d, BE_d, AG_d = dev_in[i]
+        N.gdn_tree_verify(gs.dims, w.layers, sc, X_d, gs.conv_w, BE_d, AG_d, gs.state, gs.conv_state, out[i],
                           gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
-        o_host.copy_(gs.out_o, non_blocking=True)
+        cmp_done[k].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(cmp_done[k])
+            o_host[i].copy_(out[i], non_blocking=True)
+            d2h_done[k].record(s_d2h)
         units += units_per_step[s]
-    e1.record(stream)
+    s_d2h.wait_event(d2h_done[steps - 1])
+    e1.record(s_d2h)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1)
     return dict(ms=ms, units=units, steps=steps, h2d=h2d, d2h=d2h)

@@ -43,6 +43,8 @@
 // for bit, the state the earlier verify stored for that node.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -346,6 +348,125 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   const size_t slot_stride = static_cast<size_t>(p.Hv) * tile;
   const u64 zero2 = pack2(0.f, 0.f);
 
+  bool preloaded = false;        // the tile already holds this chain's source (loaded during the last leaf)
+  // One node; the leaf flag and the "decay into the tile" flag are compile-time so each
+  // combination is its own straight-line body (no predicated rare paths on common nodes).
+  auto step = [&](int node, int c, auto leaf_t, auto low_t) {
+    constexpr bool kLeaf = decltype(leaf_t)::value;
+    constexpr bool kLow = decltype(low_t)::value;
+    const float* kvec = sm + L.kq(node);
+    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
+    const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(kvec + DK + row0);
+
+    // pass A on the state before this node
+    u64 ak[kCols], aq[kCols];
+#pragma unroll
+    for (int cc = 0; cc < kCols; ++cc) ak[cc] = aq[cc] = zero2;
+#pragma unroll
+    for (int j4 = 0; j4 < NP / 2; ++j4) {
+      const ulonglong2 kk = k4[j4];
+      const ulonglong2 qq = q4[j4];
+#pragma unroll
+      for (int cc = 0; cc < kCols; ++cc) {
+        ak[cc] = fma2(T[cc][2 * j4 + 0], kk.x, ak[cc]);
+        aq[cc] = fma2(T[cc][2 * j4 + 0], qq.x, aq[cc]);
+        ak[cc] = fma2(T[cc][2 * j4 + 1], kk.y, ak[cc]);
+        aq[cc] = fma2(T[cc][2 * j4 + 1], qq.y, aq[cc]);
+      }
+    }
+    // A chain ends at a leaf: its updated state is never read (leaves are not boundaries, and the
+    // fold rebuilds from the factor bank), so the tile is free after pass A -- start loading the
+    // next chain's source now, under this node's reduction.
+    if constexpr (kLeaf) {
+      if (c + 1 < n_chains) {
+        const int nsrc = csrc[c + 1];
+        if (nsrc >= 0 && nsrc < p.nb_max) {
+          load_tile(bnd_base + static_cast<size_t>(nsrc) * slot_stride);
+          preloaded = true;
+        }
+      }
+    }
+    float4 sk, sq;
+    {
+      const float2 a0 = unpack2(ak[0]), a1 = unpack2(ak[1]), a2 = unpack2(ak[2]), a3 = unpack2(ak[3]);
+      const float2 b0 = unpack2(aq[0]), b1 = unpack2(aq[1]), b2 = unpack2(aq[2]), b3 = unpack2(aq[3]);
+      sk = make_float4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y);
+      sq = make_float4(b0.x + b0.y, b1.x + b1.y, b2.x + b2.y, b3.x + b3.y);
+    }
+    // row groups of this warp
+#pragma unroll
+    for (int m = CG; m < 32; m <<= 1) {
+      sk.x += __shfl_xor_sync(0xffffffffu, sk.x, m);
+      sk.y += __shfl_xor_sync(0xffffffffu, sk.y, m);
+      sk.z += __shfl_xor_sync(0xffffffffu, sk.z, m);
+      sk.w += __shfl_xor_sync(0xffffffffu, sk.w, m);
+      sq.x += __shfl_xor_sync(0xffffffffu, sq.x, m);
+      sq.y += __shfl_xor_sync(0xffffffffu, sq.y, m);
+      sq.z += __shfl_xor_sync(0xffffffffu, sq.z, m);
+      sq.w += __shfl_xor_sync(0xffffffffu, sq.w, m);
+    }
+    // warps: partials [parity][warp][k|q][cpb]
+    float* part = sm + L.part0() + parity * (nwarps * 2 * cpb);
+    if (lane < CG) {
+      *reinterpret_cast<float4*>(part + (warp * 2 + 0) * cpb + c0) = sk;
+      *reinterpret_cast<float4*>(part + (warp * 2 + 1) * cpb + c0) = sq;
+    }
+    __syncthreads();
+    sk = *reinterpret_cast<const float4*>(part + c0);
+#pragma unroll
+    for (int w = 1; w < nwarps; ++w) {
+      const float4 t = *reinterpret_cast<const float4*>(part + (w * 2) * cpb + c0);
+      sk.x += t.x; sk.y += t.y; sk.z += t.z; sk.w += t.w;
+    }
+    parity ^= 1;
+    const float g = gam * sm[L.g() + node];   // gamma' of this node
+    const float bt = sm[L.beta() + node];
+    const float4 v = *reinterpret_cast<const float4*>(sm + L.v(node) + c0);
+    float4 u;
+    u.x = bt * (v.x - g * sk.x);
+    u.y = bt * (v.y - g * sk.y);
+    u.z = bt * (v.z - g * sk.z);
+    u.w = bt * (v.w - g * sk.w);
+    const size_t row = nrow0 + node;
+    if (rg == 0) {
+      sq = *reinterpret_cast<const float4*>(part + cpb + c0);
+#pragma unroll
+      for (int w = 1; w < nwarps; ++w) {
+        const float4 t = *reinterpret_cast<const float4*>(part + (w * 2 + 1) * cpb + c0);
+        sq.x += t.x; sq.y += t.y; sq.z += t.z; sq.w += t.w;
+      }
+      const float kq = sm[L.kqdot() + node];
+      float4 o;
+      o.x = fmaf(u.x, kq, g * sq.x);
+      o.y = fmaf(u.y, kq, g * sq.y);
+      o.z = fmaf(u.z, kq, g * sq.z);
+      o.w = fmaf(u.w, kq, g * sq.w);
+      *reinterpret_cast<float4*>(p.out_o + (row * p.Hv + h) * p.dv + col) = o;
+      *reinterpret_cast<float4*>(p.u_out + (row * p.Hv + h) * p.dv + col) = u;
+    }
+
+    if constexpr (!kLeaf) {   // pass B (a leaf's new state is never used)
+      float r = 1.f;
+      if constexpr (kLow) {
+        materialise(g);        // the decay goes into the tile, as in advance()
+        gam = 1.f;
+      } else {
+        r = __frcp_rn(g);
+        gam = g;
+      }
+      update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
+    }
+    if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
+    const int slot = bslot[node];
+    if (slot >= p.nb_max || (kLeaf && slot >= 0)) {   // a boundary node has children: never a leaf
+      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+    } else if (slot >= 0) {
+      store_scaled(bnd_base + static_cast<size_t>(slot) * slot_stride, gam);
+    }
+  };
+  using kT = std::true_type;
+  using kF = std::false_type;
+
   for (int c = 0; c < n_chains; ++c) {
     const int src = csrc[c];
     const int i0 = coff[c], i1 = coff[c + 1];
@@ -354,101 +475,23 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       return;
     }
     if (src >= 0) {
-      load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
+      if (!preloaded) load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
       gam = 1.f;
     }
+    preloaded = false;
     for (int i = i0; i < i1; ++i) {
       const int node = cnodes[i];
       if (node < 0 || node >= n) {
         if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
         return;
       }
-      const float* kvec = sm + L.kq(node);
-      const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
-      const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(kvec + DK + row0);
-
-      // pass A on the state before this node
-      u64 ak[kCols], aq[kCols];
-#pragma unroll
-      for (int cc = 0; cc < kCols; ++cc) ak[cc] = aq[cc] = zero2;
-#pragma unroll
-      for (int j4 = 0; j4 < NP / 2; ++j4) {
-        const ulonglong2 kk = k4[j4];
-        const ulonglong2 qq = q4[j4];
-#pragma unroll
-        for (int cc = 0; cc < kCols; ++cc) {
-          ak[cc] = fma2(T[cc][2 * j4 + 0], kk.x, ak[cc]);
-          aq[cc] = fma2(T[cc][2 * j4 + 0], qq.x, aq[cc]);
-          ak[cc] = fma2(T[cc][2 * j4 + 1], kk.y, ak[cc]);
-          aq[cc] = fma2(T[cc][2 * j4 + 1], qq.y, aq[cc]);
-        }
-      }
-      float4 sk, sq;
-      {
-        const float2 a0 = unpack2(ak[0]), a1 = unpack2(ak[1]), a2 = unpack2(ak[2]), a3 = unpack2(ak[3]);
-        const float2 b0 = unpack2(aq[0]), b1 = unpack2(aq[1]), b2 = unpack2(aq[2]), b3 = unpack2(aq[3]);
-        sk = make_float4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y);
-        sq = make_float4(b0.x + b0.y, b1.x + b1.y, b2.x + b2.y, b3.x + b3.y);
-      }
-      // row groups of this warp
-#pragma unroll
-      for (int m = CG; m < 32; m <<= 1) {
-        sk.x += __shfl_xor_sync(0xffffffffu, sk.x, m);
-        sk.y += __shfl_xor_sync(0xffffffffu, sk.y, m);
-        sk.z += __shfl_xor_sync(0xffffffffu, sk.z, m);
-        sk.w += __shfl_xor_sync(0xffffffffu, sk.w, m);
-        sq.x += __shfl_xor_sync(0xffffffffu, sq.x, m);
-        sq.y += __shfl_xor_sync(0xffffffffu, sq.y, m);
-        sq.z += __shfl_xor_sync(0xffffffffu, sq.z, m);
-        sq.w += __shfl_xor_sync(0xffffffffu, sq.w, m);
-      }
-      // warps: partials [parity][warp][k|q][cpb]
-      float* part = sm + L.part0() + parity * (nwarps * 2 * cpb);
-      if (lane < CG) {
-        *reinterpret_cast<float4*>(part + (warp * 2 + 0) * cpb + c0) = sk;
-        *reinterpret_cast<float4*>(part + (warp * 2 + 1) * cpb + c0) = sq;
-      }
-      __syncthreads();
-      sk = *reinterpret_cast<const float4*>(part + c0);
-#pragma unroll
-      for (int w = 1; w < nwarps; ++w) {
-        const float4 t = *reinterpret_cast<const float4*>(part + (w * 2) * cpb + c0);
-        sk.x += t.x; sk.y += t.y; sk.z += t.z; sk.w += t.w;
-      }
-      parity ^= 1;
-      const float g = gam * sm[L.g() + node];   // gamma' of this node
-      const float bt = sm[L.beta() + node];
-      const float4 v = *reinterpret_cast<const float4*>(sm + L.v(node) + c0);
-      float4 u;
-      u.x = bt * (v.x - g * sk.x);
-      u.y = bt * (v.y - g * sk.y);
-      u.z = bt * (v.z - g * sk.z);
-      u.w = bt * (v.w - g * sk.w);
-      const size_t row = nrow0 + node;
-      if (rg == 0) {
-        sq = *reinterpret_cast<const float4*>(part + cpb + c0);
-#pragma unroll
-        for (int w = 1; w < nwarps; ++w) {
-          const float4 t = *reinterpret_cast<const float4*>(part + (w * 2 + 1) * cpb + c0);
-          sq.x += t.x; sq.y += t.y; sq.z += t.z; sq.w += t.w;
-        }
-        const float kq = sm[L.kqdot() + node];
-        float4 o;
-        o.x = fmaf(u.x, kq, g * sq.x);
-        o.y = fmaf(u.y, kq, g * sq.y);
-        o.z = fmaf(u.z, kq, g * sq.z);
-        o.w = fmaf(u.w, kq, g * sq.w);
-        *reinterpret_cast<float4*>(p.out_o + (row * p.Hv + h) * p.dv + col) = o;
-        *reinterpret_cast<float4*>(p.u_out + (row * p.Hv + h) * p.dv + col) = u;
-      }
-
-      gam = advance(kvec, g, u);   // pass B
-      if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
-      const int slot = bslot[node];
-      if (slot >= p.nb_max) {
-        if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-      } else if (slot >= 0) {
-        store_scaled(bnd_base + static_cast<size_t>(slot) * slot_stride, gam);
+      const bool low = gam * sm[L.g() + node] < kGammaFloor;
+      if (i == i1 - 1) {
+        if (low) step(node, c, kT{}, kT{});
+        else step(node, c, kT{}, kF{});
+      } else {
+        if (low) step(node, c, kF{}, kT{});
+        else step(node, c, kF{}, kF{});
       }
     }
   }
