@@ -39,6 +39,31 @@ METRIC = "verified tree-nodes/sec (GDN layer·head·node) and achieved HBM GB/s 
 UNIT = "nodes/s"
 
 
+def measured_traffic():
+    """DRAM bytes per verify call from the committed ncu capture, if the kernels have not changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_gdn_tree_verify_batched32x48.txt")
+    try:
+        fields = {}
+        for line in open(path):
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split()
+            fields[parts[0]] = parts[1]
+        csrc = os.path.join(ROOT, "gated_deltanet_tree_gb300", "csrc")
+        h = hashlib.sha256()
+        for f in sorted(os.listdir(csrc)):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+        with open(os.path.join(ROOT, "include", "gdn_tree.h"), "rb") as fh:
+            h.update(fh.read())
+        if h.hexdigest() != fields.get("source_sha256"):
+            return None
+        return float(fields["traffic_bytes_per_call"])
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -483,7 +508,8 @@ def main():
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
-                     "avg_launch_ms": statistics.mean(r["verify_ms"]), "traffic": None},
+                     "avg_launch_ms": statistics.mean(r["verify_ms"]),
+                     "traffic": measured_traffic() if w.cfg == 4 and w.B == 32 and w.layers == 48 else None},
         "finish_ms": r["finish_ms"],
         "clocks": r["clocks"],
         "e2e": None if args.no_e2e else {
