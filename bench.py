@@ -353,6 +353,11 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     finish_ms = f0.elapsed_time(f1)
 
     # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
+    # A/B: the same steps with per-node-state schedules (every node reloads its parent's stored state)
+    ab = None
+    if not args.no_ab:
+        ab = run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_step)
+
     if args.no_e2e:
         e2e = dict(ms=float("nan"), units=0, steps=0, h2d=0, d2h=0)
     else:
@@ -365,10 +370,52 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     avg_verify_s = statistics.mean(verify_ms) / 1e3
     avg_bytes = statistics.mean(timed_bytes)
     achieved = avg_bytes / avg_verify_s / 1e9
-    return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk,
+    return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap,
                 gpu_launches=args.steps * 3)
+
+
+def run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_step):
+    """Per-node-state baseline on the same workload: schedules with no heavy edges, every node with
+    children stored and reloaded (the snapshot-style traffic the heavy-light chains avoid)."""
+    import torch
+    from gated_deltanet_tree_gb300 import _native as N
+    steps = max(2, min(args.steps, 10))
+    packed, nb_cap = [], 1
+    for s in range(w.steps):
+        P, n = parents_host[s]
+        words, nb = N.gdn_pack_schedules_per_node(P, n)
+        packed.append(torch.from_numpy(words).to(dev))
+        nb_cap = max(nb_cap, nb)
+    boundary = torch.empty(w.B, w.layers, nb_cap, w.Hv, w.dk, w.dv, dtype=torch.float32, device=dev)
+    ver = gs.ver
+
+    def one(i):
+        s = i % w.steps
+        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=nb_cap, words=packed[s].data_ptr())
+        X, BE, AG = gs.inputs[s]
+        N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
+                          boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+        N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    units = 0
+    for i in range(3, 3 + steps):
+        one(i)
+        units += int(parents_host[i % w.steps][1].sum()) * w.layers * w.Hv
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ver.check_error()
+    ms = e0.elapsed_time(e1)
+    del boundary
+    torch.cuda.empty_cache()
+    return {"schedule": "per-node states (no heavy edges)", "steps": steps, "nb_max": nb_cap,
+            "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
 
 def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct, units_per_step):
@@ -447,6 +494,7 @@ def main():
     ap.add_argument("--requests", type=int, default=None, help="override requests per GPU (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=None, help="override GDN layers (smaller profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ab", action="store_true", help="skip the per-node-state A/B run")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -516,6 +564,8 @@ def main():
             "value": r["e2e_units"] / (r["e2e_ms"] / 1e3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
         "gpu_launches": r["gpu_launches"],
+        "ab_per_node_states": None if r["ab"] is None else dict(
+            r["ab"], hld_speedup=r["ab"]["ms_per_step"] / (r["ms"] / args.steps)),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -82,6 +82,7 @@ def lib():
         L.gdn_schedule_words.argtypes = [c_i32]
         L.gdn_schedule_words.restype = c_i32
         L.gdn_pack_schedules.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
+        L.gdn_pack_schedules_per_node.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
         L.gdn_banks_init.argtypes = [P(gdn_banks), c_i32, c_i32, c_i32]
         L.gdn_workspace_bytes.argtypes = [P(gdn_dims), c_i32, c_i32, c_i32]
         L.gdn_workspace_bytes.restype = ctypes.c_size_t
@@ -92,7 +93,7 @@ def lib():
         L.gdn_commit_fold.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_i32, P(gdn_banks), c_p]
         L.gdn_finish.argtypes = [P(gdn_dims), c_i32, c_i32, c_p, c_p, P(gdn_banks), c_p]
         L.gdn_check_error.argtypes = [P(gdn_banks), c_p]
-        for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_banks_init", "gdn_tree_verify",
+        for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_pack_schedules_per_node", "gdn_banks_init", "gdn_tree_verify",
                      "gdn_tree_verify_noalloc", "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
             getattr(L, name).restype = c_i32
         _lib = L
@@ -161,6 +162,19 @@ def gdn_pack_schedules(parents: np.ndarray, n: np.ndarray):
     P = ctypes.POINTER(c_i32)
     _check(lib().gdn_pack_schedules(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max,
                                     words.ctypes.data_as(P), ctypes.byref(nb)))
+    return words, int(nb.value)
+
+
+def gdn_pack_schedules_per_node(parents: np.ndarray, n: np.ndarray):
+    """Per-node-state schedule (every node its own chain) in the packed layout -> (words, nb_max)."""
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    n = np.ascontiguousarray(n, dtype=np.int32)
+    B, n_max = parents.shape
+    words = np.empty((B, gdn_schedule_words(n_max)), dtype=np.int32)
+    nb = c_i32(0)
+    P = ctypes.POINTER(c_i32)
+    _check(lib().gdn_pack_schedules_per_node(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max,
+                                             words.ctypes.data_as(P), ctypes.byref(nb)))
     return words, int(nb.value)
 
 

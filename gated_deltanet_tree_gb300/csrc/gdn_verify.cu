@@ -486,7 +486,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         return;
       }
       const bool low = gam * sm[L.g() + node] < kGammaFloor;
-      if (i == i1 - 1) {
+      // the last node of a chain whose state nobody reads: a leaf (HLD chains always end at one; a
+      // schedule may also end a chain at a boundary node, whose state is stored)
+      if (i == i1 - 1 && bslot[node] < 0) {
         if (low) step(node, c, kT{}, kT{});
         else step(node, c, kT{}, kF{});
       } else {

@@ -142,6 +142,69 @@ extern "C" gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_sch
 
 extern "C" int32_t gdn_schedule_words(int32_t n_max) { return gdn::SchedLayout{n_max}.words(); }
 
+// Per-node-state schedule: no heavy edges, every node its own chain, every node with children
+// materialised; chains ordered by (depth, node).  Same packed layout as the heavy-light one.
+static gdn_status pack_per_node(const int32_t* parent, int n, const gdn::SchedLayout& lay, int32_t* w,
+                                int* nb_out) {
+  if (n < 1 || parent[0] != -1) return fail(GDN_ERR_INVALID_TREE, "parent[0] must be -1");
+  std::vector<int32_t> depth(n, 0), kids(n, 0);
+  for (int i = 1; i < n; ++i) {
+    if (parent[i] < 0 || parent[i] >= i) return fail(GDN_ERR_INVALID_TREE, "parent[%d] = %d", i, parent[i]);
+    depth[i] = depth[parent[i]] + 1;
+    kids[parent[i]]++;
+  }
+  int max_depth = 0;
+  for (int i = 0; i < n; ++i) max_depth = depth[i] > max_depth ? depth[i] : max_depth;
+  std::vector<int32_t> order;
+  for (int d = 0; d <= max_depth; ++d)
+    for (int i = 0; i < n; ++i)
+      if (depth[i] == d) order.push_back(i);
+  std::vector<int32_t> slot(n, -1);
+  int nb = 0;
+  for (int i = 0; i < n; ++i)
+    if (kids[i] > 0) slot[i] = nb++;
+  for (int i = 0; i < lay.words(); ++i) w[i] = -1;
+  w[0] = n;
+  w[1] = n;
+  w[2] = nb;
+  w[3] = max_depth + 1;
+  for (int i = 0; i < n; ++i) {
+    w[lay.parent() + i] = parent[i];
+    w[lay.bslot() + i] = slot[i];
+  }
+  for (int c = 0; c < n; ++c) {
+    const int v = order[c];
+    w[lay.chain_src() + c] = v == 0 ? -1 : slot[parent[v]];
+    w[lay.chain_off() + c] = c;
+    w[lay.chain_nodes() + c] = v;
+  }
+  w[lay.chain_off() + n] = n;
+  *nb_out = nb;
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const int32_t* n, int32_t B,
+                                                  int32_t n_max, int32_t* words, int32_t* nb_max_out) {
+  gdn::clear_error();
+  if (!parents || !n || !words) return fail(GDN_ERR_INVALID_ARG, "NULL argument to gdn_pack_schedules_per_node");
+  if (B < 1) return fail(GDN_ERR_INVALID_ARG, "B = %d", B);
+  if (n_max < 1 || n_max > GDN_MAX_NODES)
+    return fail(GDN_ERR_UNSUPPORTED, "n_max = %d outside 1..%d", n_max, GDN_MAX_NODES);
+  const gdn::SchedLayout lay{n_max};
+  int nb_max = 0;
+  for (int b = 0; b < B; ++b) {
+    if (n[b] < 1 || n[b] > n_max)
+      return fail(GDN_ERR_INVALID_TREE, "request %d: n = %d outside 1..n_max (%d)", b, n[b], n_max);
+    int nb = 0;
+    gdn_status st = pack_per_node(parents + static_cast<size_t>(b) * n_max, n[b], lay,
+                                  words + static_cast<size_t>(b) * lay.words(), &nb);
+    if (st != GDN_OK) return st;
+    nb_max = nb > nb_max ? nb : nb_max;
+  }
+  if (nb_max_out) *nb_max_out = nb_max;
+  return GDN_OK;
+}
+
 extern "C" gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
                                          int32_t* words, int32_t* nb_max_out) {
   gdn::clear_error();

@@ -27,14 +27,15 @@ class DeviceSchedule:
     """A packed batch schedule resident on the device."""
 
     def __init__(self, parents: Sequence[np.ndarray], n_max: int, device, nb_cap: Optional[int] = None,
-                 words_out: Optional[torch.Tensor] = None, stream=None):
+                 words_out: Optional[torch.Tensor] = None, stream=None, per_node: bool = False):
         B = len(parents)
         P = np.full((B, n_max), -1, dtype=np.int32)
         n = np.zeros(B, dtype=np.int32)
         for b, p in enumerate(parents):
             P[b, :len(p)] = p
             n[b] = len(p)
-        words, nb = N.gdn_pack_schedules(P, n)
+        pack = N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules
+        words, nb = pack(P, n)
         self.parents, self.n, self.nb_max = P, n, nb if nb_cap is None else max(nb, nb_cap)
         if words_out is None:
             self.words = torch.from_numpy(words).to(device)
@@ -89,8 +90,9 @@ class TreeVerifier:
         raise KeyError(field)
 
     # calls ---------------------------------------------------------------------
-    def schedule(self, parents: Sequence[np.ndarray], nb_cap: Optional[int] = None) -> DeviceSchedule:
-        return DeviceSchedule(parents, self.n_max, self.device, nb_cap)
+    def schedule(self, parents: Sequence[np.ndarray], nb_cap: Optional[int] = None,
+                 per_node: bool = False) -> DeviceSchedule:
+        return DeviceSchedule(parents, self.n_max, self.device, nb_cap, per_node=per_node)
 
     def verify(self, sched: DeviceSchedule, x_raw, conv_w, beta, log_g, state, conv_state, out_o, boundary,
                stream=None):

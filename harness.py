@@ -31,8 +31,9 @@ class WorkloadPlan:
     """Trees and accepted paths of every step (host), generated up front."""
 
     def __init__(self, w: S.Workload, trees: Optional[List[List[np.ndarray]]] = None,
-                 paths: Optional[List[List[np.ndarray]]] = None):
+                 paths: Optional[List[List[np.ndarray]]] = None, per_node: bool = False):
         self.w = w
+        self.per_node = per_node   # per-node-state schedules instead of heavy-light ones
         self.trees = trees if trees is not None else [S.step_trees(w, s) for s in range(w.steps)]
         self.paths = paths if paths is not None else [S.step_paths(w, self.trees[s], s) for s in range(w.steps)]
         self.nb_cap = 0
@@ -42,7 +43,7 @@ class WorkloadPlan:
             for b, p in enumerate(self.trees[s]):
                 P[b, :len(p)] = p
                 n[b] = len(p)
-            _, nb = N.gdn_pack_schedules(P, n)
+            _, nb = (N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules)(P, n)
             self.nb_cap = max(self.nb_cap, nb)
 
 
@@ -98,7 +99,8 @@ class GpuSession:
 
     def schedule(self, step: int) -> DeviceSchedule:
         if step not in self.scheds:
-            self.scheds[step] = self.ver.schedule(self.plan.trees[step], nb_cap=self.nb_cap)
+            self.scheds[step] = self.ver.schedule(self.plan.trees[step], nb_cap=self.nb_cap,
+                                                  per_node=self.plan.per_node)
         return self.scheds[step]
 
     def paths(self, step: int):

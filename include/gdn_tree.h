@@ -131,6 +131,15 @@ int32_t gdn_schedule_words(int32_t n_max);
 gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
                               int32_t* words_host, int32_t* nb_max_out);
 
+/* Per-node-state schedule in the same packed layout, for comparison with the heavy-light one: no heavy
+ * edges, every node its own chain (ordered by depth, then node), every node with children materialised
+ * in a boundary slot.  The verify then reloads and stores a state at every step of the tree -- the
+ * rollback-by-snapshot scheme the SpecLA article replaces ("状态驻留验证": state traffic twice per
+ * token instead of twice per chain).  Same arguments and results as gdn_pack_schedules; nb_max is the
+ * number of nodes with children. */
+gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
+                                       int32_t* words_host, int32_t* nb_max_out);
+
 typedef struct {
   int32_t B;               /* requests */
   int32_t n_max;           /* node stride of every per-node array */

@@ -39,6 +39,10 @@ class OracleUnit:
         n = len(parent)
         X, BE, AG = unit_inputs(self.w, self.b, self.l, step, n)
         sched = O.hld_schedule(parent)
+        if getattr(self.plan, "per_node", False):
+            # per-node-state schedule: every node with children is materialised, slots in node order
+            internal = sorted({int(v) for v in parent[1:]})
+            sched = dict(sched, boundary_node=internal, n_boundary=len(internal))
         exp = self.sess.verify(parent, X, BE, AG, sched["boundary_node"])
         exp["T"], exp["W"] = self.sess.committed()
         exp["n"], exp["sched"] = n, sched

@@ -190,3 +190,30 @@ def test_workspace_bytes(N):
     got = N.gdn_workspace_bytes(d, 32, 48, 22)
     rows = 32 * 48 * 22
     assert got >= rows * (16 * 128 + 48 * 128) * 4 and got % 256 == 0
+
+
+def test_per_node_schedule_layout(N):
+    rng = np.random.default_rng(9)
+    n_max = 20
+    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(8)] + [S.chain_tree(n_max)]
+    P = np.full((len(trees), n_max), -1, dtype=np.int32)
+    n = np.array([len(t) for t in trees], dtype=np.int32)
+    for b, t in enumerate(trees):
+        P[b, :len(t)] = t
+    words, nb_max = N.gdn_pack_schedules_per_node(P, n)
+    for b, t in enumerate(trees):
+        m, w = len(t), words[b]
+        kids = np.bincount(t[1:], minlength=m) if m > 1 else np.zeros(1, dtype=int)
+        internal = [v for v in range(m) if kids[v] > 0]
+        assert list(w[:3]) == [m, m, len(internal)]
+        bslot = list(w[4 + n_max:4 + n_max + m])
+        assert [v for v in range(m) if bslot[v] >= 0] == internal
+        order = list(w[5 + 4 * n_max:5 + 4 * n_max + m])
+        depth = [len(O.root_path(t, v)) - 1 for v in range(m)]
+        assert order == sorted(range(m), key=lambda v: (depth[v], v))
+        src = list(w[4 + 2 * n_max:4 + 2 * n_max + m])
+        for c, v in enumerate(order):
+            assert src[c] == (-1 if v == 0 else bslot[t[v]])
+        assert list(w[4 + 3 * n_max:5 + 3 * n_max + m]) == list(range(m + 1))
+        assert all(x == -1 for x in w[5 + 5 * n_max:5 + 5 * n_max + m])     # no heavy edges
+    assert nb_max == max(int((np.bincount(t[1:], minlength=len(t)) > 0).sum()) if len(t) > 1 else 0 for t in trees)

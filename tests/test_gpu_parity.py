@@ -130,6 +130,15 @@ def test_compaction_is_exact_and_transparent():
     gs, _ = run_parity(w, compact_steps=(0, 1, 2, 3))
 
 
+@pytest.mark.parametrize("cfg", [1, 2], ids=["tiny", "qwen"])
+def test_per_node_state_schedule(cfg):
+    # the per-node-state baseline (every node reloads its parent's stored state) gives the same results
+    from harness import WorkloadPlan
+    w = S.workload(cfg).replace(steps=3, B=2) if cfg == 1 else S.workload(cfg).replace(steps=3)
+    plan = WorkloadPlan(w, per_node=True)
+    run_parity(w, plan=plan)
+
+
 def test_qwen_like_single_layer():
     w = S.workload(2).replace(steps=3)
     run_parity(w)
