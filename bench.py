@@ -78,8 +78,17 @@ def peaks():
 # once, every output written once)
 # ----------------------------------------------------------------------------
 
+def hbm_stashes(words: np.ndarray, n_max: int):
+    """Per request: the stashes a packed schedule writes to HBM (ops with the boundary-slot push bit);
+    with boundary states as scratch, the others stay in tensor memory."""
+    ops = words[:, 5 + 3 * n_max:5 + 4 * n_max]
+    n = words[:, 0]
+    return [int(((ops[b, :n[b]] >> 12) & 3 == 3).sum()) for b in range(words.shape[0])]
+
+
 def algorithmic_bytes(w: S.Workload, n_per_req, nb_per_req, pend_len_per_req):
-    """Compulsory bytes of one gdn_tree_verify call (conv window + chain verify)."""
+    """Compulsory bytes of one gdn_tree_verify call (conv window + chain verify); nb_per_req = the
+    state tiles each request writes beside its committed state (stored boundary states or HBM stashes)."""
     ib = 2 if w.in_dtype == S.DTYPE_BF16 else 4
     tile = w.dk * w.dv * 4 * w.Hv                    # all v-heads of one (request, layer)
     C = w.C
@@ -99,6 +108,20 @@ def algorithmic_bytes(w: S.Workload, n_per_req, nb_per_req, pend_len_per_req):
     if w.conv_mode:
         total += w.layers * C * w.K * 4               # conv weights
     return total
+
+
+def algorithmic_fma(w: S.Workload, n_per_req, leaves_per_req, pend_len_per_req):
+    """FP32 multiply-adds of one verify call on the state tiles: per node T^T k and T^T q (2 per element),
+    the update (1 per element, not for leaves, whose new state is never read), 1 per element per folded
+    node.  The per-node vector work (u, o, normalisation, conv) is a few hundred operations per head and
+    is left out."""
+    per_elem = sum(2 * n + (n - lv) + L for n, lv, L in zip(n_per_req, leaves_per_req, pend_len_per_req))
+    return per_elem * w.layers * w.Hv * w.dk * w.dv
+
+
+def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
+    """Dense FP32 FMA peak: 128 FP32 lanes per SM, 2 flops per FMA."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ----------------------------------------------------------------------------
@@ -299,7 +322,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         if timing is not None:
             timing[0].record(stream)
         N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
-                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, stream)
         if timing is not None:
             timing[1].record(stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
@@ -309,15 +332,18 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
             dist.barrier()
 
     # bytes / units of each step (pending length of step s = accepted path length of step s-1)
-    units_per_step, bytes_per_step = [], []
+    units_per_step, bytes_per_step, fma_per_step = [], [], []
     for i in range(args.warmup + args.steps):
         s = i % w.steps
         n_req = [len(p) for p in plan.trees[s]]
-        nb_req = [int(N.gdn_hld_schedule(p)["n_boundary"]) for p in plan.trees[s]]
+        P, n = parents_host[s]
+        nb_req = hbm_stashes(N.gdn_pack_schedules(P, n)[0], w.n_max)   # boundary states are scratch
         prev = plan.paths[(i - 1) % w.steps] if i > 0 else [[] for _ in range(w.B)]
         L_req = [len(p) for p in prev]
         units_per_step.append(sum(n_req) * w.layers * w.Hv)
         bytes_per_step.append(algorithmic_bytes(w, n_req, nb_req, L_req))
+        leaves = [int((np.bincount(p[1:], minlength=len(p)) == 0).sum()) if len(p) > 1 else 1 for p in plan.trees[s]]
+        fma_per_step.append(algorithmic_fma(w, n_req, leaves, L_req))
 
     for i in range(args.warmup):
         one_step(i)
@@ -370,8 +396,12 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     avg_verify_s = statistics.mean(verify_ms) / 1e3
     avg_bytes = statistics.mean(timed_bytes)
     achieved = avg_bytes / avg_verify_s / 1e9
+    avg_flops = 2 * statistics.mean(fma_per_step[args.warmup:])
+    alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
+                                (clk or {}).get("sm_max_mhz") or 2070.0)
     return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
+                avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap,
                 gpu_launches=args.steps * 3)
 
@@ -396,7 +426,7 @@ def run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_ste
         sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=nb_cap, words=packed[s].data_ptr())
         X, BE, AG = gs.inputs[s]
         N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
-                          boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+                          boundary, ver.banks, ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
 
     for i in range(3):
@@ -467,7 +497,7 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
         sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, words=wd[i].data_ptr())
         X_d, BE_d, AG_d = dev_in[i]
         N.gdn_tree_verify(gs.dims, w.layers, sc, X_d, gs.conv_w, BE_d, AG_d, gs.state, gs.conv_state, out[i],
-                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, stream)
+                          gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
         cmp_done[k].record(stream)
         with torch.cuda.stream(s_d2h):
@@ -552,12 +582,18 @@ def main():
         "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 (bf16 inputs)", "data": "synthetic (seeded DDTree-shaped trees, "
         "random activations; no model weights)", "config": config,
-        "roofline": {"bound": "hbm", "kernel": "gdn_tree_verify (conv_window_kernel + chain_verify_kernel)",
+        "roofline": {"bound": "hbm" if r["avg_bytes"] / (r["peak"] * 1e9) >= r["avg_flops"] / (r["alu_peak"] * 1e12)
+                     else "alu",
+                     "kernel": "gdn_tree_verify (conv_window_kernel + chain_verify_kernel)",
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
                      "avg_launch_ms": statistics.mean(r["verify_ms"]),
-                     "traffic": measured_traffic() if w.cfg == 4 and w.B == 32 and w.layers == 48 else None},
+                     "traffic": measured_traffic() if w.cfg == 4 and w.B == 32 and w.layers == 48 else None,
+                     "alu": {"achieved": r["avg_flops"] / r["avg_verify_s"] / 1e12, "peak": r["alu_peak"],
+                             "unit": "TFLOP/s", "frac": r["avg_flops"] / r["avg_verify_s"] / 1e12 / r["alu_peak"],
+                             "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x max SM clock",
+                             "algorithmic_flops_per_launch": r["avg_flops"]}},
         "finish_ms": r["finish_ms"],
         "clocks": r["clocks"],
         "e2e": None if args.no_e2e else {

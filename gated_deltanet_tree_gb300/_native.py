@@ -31,6 +31,7 @@ GDN_ERR_SCHEDULE = -9
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_COMMIT_COMPACT = 1
+GDN_VERIFY_BOUNDARY_SCRATCH = 1
 GDN_MAX_NODES = 64
 
 
@@ -83,17 +84,22 @@ def lib():
         L.gdn_schedule_words.restype = c_i32
         L.gdn_pack_schedules.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
         L.gdn_pack_schedules_per_node.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
+        L.gdn_ddtree_build.argtypes = [P(ctypes.c_float), c_i32, c_i32, c_i32, ctypes.c_double, c_i32, P(c_i32),
+                                       P(c_i32), P(c_i32), P(ctypes.c_double), P(c_i32)]
+        L.gdn_ddtree_build_batch.argtypes = [P(ctypes.c_float), c_i32, c_i32, c_i32, c_i32, ctypes.c_double, c_i32,
+                                             c_i32, P(c_i32), P(c_i32)]
         L.gdn_banks_init.argtypes = [P(gdn_banks), c_i32, c_i32, c_i32]
         L.gdn_workspace_bytes.argtypes = [P(gdn_dims), c_i32, c_i32, c_i32]
         L.gdn_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_tree_verify.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
-                                      c_p, P(gdn_banks), c_p, ctypes.c_size_t, c_p]
+                                      c_p, P(gdn_banks), c_p, ctypes.c_size_t, c_i32, c_p]
         L.gdn_tree_verify_noalloc.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_p, c_p, c_p,
-                                              c_p, c_p, c_p, P(gdn_banks), c_p]
+                                              c_p, c_p, c_p, P(gdn_banks), c_i32, c_p]
         L.gdn_commit_fold.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_i32, P(gdn_banks), c_p]
         L.gdn_finish.argtypes = [P(gdn_dims), c_i32, c_i32, c_p, c_p, P(gdn_banks), c_p]
         L.gdn_check_error.argtypes = [P(gdn_banks), c_p]
-        for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_pack_schedules_per_node", "gdn_banks_init", "gdn_tree_verify",
+        for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_pack_schedules_per_node", "gdn_ddtree_build",
+                     "gdn_ddtree_build_batch", "gdn_banks_init", "gdn_tree_verify",
                      "gdn_tree_verify_noalloc", "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
             getattr(L, name).restype = c_i32
         _lib = L
@@ -178,6 +184,43 @@ def gdn_pack_schedules_per_node(parents: np.ndarray, n: np.ndarray):
     return words, int(nb.value)
 
 
+GDN_DDTREE_CHAIN_SEED = 1
+
+
+def gdn_ddtree_build(logp: np.ndarray, budget: int, tau: Optional[float] = None, chain_seed: bool = True):
+    """DDTree of one draft table logp [depth_max][top_k] -> dict(parent, depth, rank, score) in DFS preorder.
+    tau None disables pruning."""
+    logp = np.ascontiguousarray(logp, dtype=np.float32)
+    depth_max, top_k = logp.shape
+    P = ctypes.POINTER(c_i32)
+    parent = np.empty(budget, dtype=np.int32)
+    depth = np.empty(budget, dtype=np.int32)
+    rank = np.empty(budget, dtype=np.int32)
+    score = np.empty(budget, dtype=np.float64)
+    n = c_i32(0)
+    _check(lib().gdn_ddtree_build(logp.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), depth_max, top_k, budget,
+                                  -1.0 if tau is None else float(tau), GDN_DDTREE_CHAIN_SEED if chain_seed else 0,
+                                  parent.ctypes.data_as(P), depth.ctypes.data_as(P), rank.ctypes.data_as(P),
+                                  score.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), ctypes.byref(n)))
+    k = int(n.value)
+    return {"parent": parent[:k].copy(), "depth": depth[:k].copy(), "rank": rank[:k].copy(), "score": score[:k].copy()}
+
+
+def gdn_ddtree_build_batch(logp: np.ndarray, budget: int, n_max: int, tau: Optional[float] = None,
+                           chain_seed: bool = True):
+    """B DDTrees from logp [B][depth_max][top_k] -> (parents [B][n_max] padded with -1, n [B])."""
+    logp = np.ascontiguousarray(logp, dtype=np.float32)
+    B, depth_max, top_k = logp.shape
+    P = ctypes.POINTER(c_i32)
+    parents = np.empty((B, n_max), dtype=np.int32)
+    n = np.empty(B, dtype=np.int32)
+    _check(lib().gdn_ddtree_build_batch(logp.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), B, depth_max, top_k,
+                                        budget, -1.0 if tau is None else float(tau),
+                                        GDN_DDTREE_CHAIN_SEED if chain_seed else 0, n_max,
+                                        parents.ctypes.data_as(P), n.ctypes.data_as(P)))
+    return parents, n
+
+
 def gdn_banks_init(banks: gdn_banks, B: int, layers: int, n_max: int):
     _check(lib().gdn_banks_init(ctypes.byref(banks), B, layers, n_max))
 
@@ -188,19 +231,20 @@ def gdn_workspace_bytes(dims: gdn_dims, B: int, layers: int, n_max: int) -> int:
 
 def gdn_tree_verify(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, x_raw, conv_w, beta, log_g, state,
                     conv_state, out_o, boundary_states, banks: gdn_banks, workspace, workspace_bytes: int,
-                    stream=None):
+                    flags: int = 0, stream=None):
     _check(lib().gdn_tree_verify(ctypes.byref(dims), layers, ctypes.byref(sched), _ptr(x_raw), _ptr(conv_w),
                                  _ptr(beta), _ptr(log_g), _ptr(state), _ptr(conv_state), _ptr(out_o),
                                  _ptr(boundary_states), ctypes.byref(banks), _ptr(workspace), workspace_bytes,
-                                 _stream(stream)))
+                                 flags, _stream(stream)))
 
 
 def gdn_tree_verify_noalloc(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, x_raw, conv_w, beta, log_g,
-                            state, conv_state, out_o, boundary_states, banks: gdn_banks, stream=None):
+                            state, conv_state, out_o, boundary_states, banks: gdn_banks, flags: int = 0,
+                            stream=None):
     """gdn_tree_verify without a workspace: the library's fixed device scratch is used instead."""
     _check(lib().gdn_tree_verify_noalloc(ctypes.byref(dims), layers, ctypes.byref(sched), _ptr(x_raw), _ptr(conv_w),
                                          _ptr(beta), _ptr(log_g), _ptr(state), _ptr(conv_state), _ptr(out_o),
-                                         _ptr(boundary_states), ctypes.byref(banks), _stream(stream)))
+                                         _ptr(boundary_states), ctypes.byref(banks), flags, _stream(stream)))
 
 
 def gdn_commit_fold(dims: gdn_dims, layers: int, sched: gdn_batch_schedule, path, length, flags: int,

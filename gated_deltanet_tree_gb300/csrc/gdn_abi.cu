@@ -147,8 +147,9 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
 gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched, const void* x_raw,
                            const float* conv_w, const void* beta, const void* log_g, float* state,
                            float* conv_state, float* out_o, float* boundary_states, gdn_banks* banks,
-                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                           void* workspace, size_t workspace_bytes, int32_t flags, cudaStream_t stream) {
   gdn::clear_error();
+  if (flags & ~GDN_VERIFY_BOUNDARY_SCRATCH) return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
   GDN_TRY(check_dims(d));
   GDN_TRY(check_sched(sched));
   if (layers < 1) return fail(GDN_ERR_INVALID_ARG, "layers = %d", layers);
@@ -195,6 +196,7 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   vp.beta = beta; vp.log_g = log_g; vp.q_in = ws_q; vp.v_in = ws_v; vp.k_in = banks->k[cur];
   vp.u_out = banks->u[cur]; vp.a_out = banks->a[cur];
   vp.state = state; vp.out_o = out_o; vp.boundary = boundary_states;
+  vp.boundary_out = (flags & GDN_VERIFY_BOUNDARY_SCRATCH) ? 0 : 1;
   vp.fold = pend >= 0;
   if (pend >= 0) {
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];

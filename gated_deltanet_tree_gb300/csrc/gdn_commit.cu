@@ -32,8 +32,9 @@ __global__ void commit_record_kernel(CommitParams p) {
   }
   int32_t* pp = p.pend_path + static_cast<size_t>(b) * p.n_max;
   if (ok) {
-    const int32_t* heavy = rec + lay.heavy();
-    for (int i = 0; i < L; ++i) pp[i] = path[i] | ((i > 0 && heavy[path[i - 1]] != path[i]) ? kPathHeadFlag : 0);
+    const int32_t* nflags = rec + lay.nflags();
+    for (int i = 0; i < L; ++i)
+      pp[i] = path[i] | ((i > 0 && (nflags[path[i - 1]] & kNodeMaterialised)) ? kPathHeadFlag : 0);
     p.pend_len[b] = L;
   } else {
     p.pend_len[b] = 0;

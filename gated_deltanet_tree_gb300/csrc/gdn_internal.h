@@ -63,18 +63,29 @@ __device__ __forceinline__ bool launch_aborted(const int32_t* err) {
 // Offsets inside one packed schedule record (see gdn_tree.h).
 struct SchedLayout {
   int n_max;
-  __host__ __device__ int words() const { return 5 + 6 * n_max; }
-  __host__ __device__ int parent() const { return 4; }
-  __host__ __device__ int bslot() const { return 4 + n_max; }
-  __host__ __device__ int chain_src() const { return 4 + 2 * n_max; }
-  __host__ __device__ int chain_off() const { return 4 + 3 * n_max; }
-  __host__ __device__ int chain_nodes() const { return 5 + 4 * n_max; }
-  __host__ __device__ int heavy() const { return 5 + 5 * n_max; }
+  __host__ __device__ int words() const { return 5 + 4 * n_max; }
+  __host__ __device__ int parent() const { return 5; }
+  __host__ __device__ int bslot() const { return 5 + n_max; }
+  __host__ __device__ int nflags() const { return 5 + 2 * n_max; }
+  __host__ __device__ int ops() const { return 5 + 3 * n_max; }
 };
 
+// One verify op per node, in the order the verify walks the tree (see gdn_tree.h).
+constexpr int32_t kOpNode = 0xFF;             // node index
+constexpr int32_t kOpReload = 1 << 8;         // start from the parent's stashed state (else: the registers)
+constexpr int32_t kOpReloadGlobal = 1 << 9;   // ... stashed in the parent's boundary slot (else: tensor memory)
+constexpr int kOpReloadLevelShift = 10;       // 2 bits: tensor-memory level of the reload
+constexpr int32_t kOpPush = 1 << 12;          // after the node: materialise and stash its state
+constexpr int32_t kOpPushGlobal = 1 << 13;    // ... in the node's boundary slot (else: tensor memory)
+constexpr int kOpPushLevelShift = 14;         // 2 bits: tensor-memory level of the push
+constexpr int32_t kOpLeaf = 1 << 16;          // no children: the node's update is never read
+constexpr int kTmemLevels = 2;                // stash levels kept in tensor memory; deeper ones spill to HBM
+// nflags bit: the state after this node is materialised (the verify stashed it)
+constexpr int32_t kNodeMaterialised = 1;
+
 // Encoding of a recorded pending-path entry: node index in the low bits; the
-// head flag marks a node that starts a new chain (its parent's light child),
-// where the verify materialised the state and reloaded it.
+// head flag marks a node entered from a materialised state (its parent's state
+// was stashed by the verify), where the fold materialises as well.
 constexpr int32_t kPathNodeMask = 0xFFFF;
 constexpr int32_t kPathHeadFlag = 1 << 30;
 
@@ -111,6 +122,7 @@ struct VerifyParams {
   float* state;                // [B][L][Hv][dk][dv]
   float* out_o;                // [B][L][n_max][Hv][dv]
   float* boundary;             // [B][L][nb_max][Hv][dk][dv]
+  int boundary_out;            // store every boundary state (else the slots only take spills)
   int fold;
   const float* pend_k;
   const float* pend_u;

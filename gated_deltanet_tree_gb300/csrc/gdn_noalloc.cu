@@ -58,7 +58,8 @@ gdn_status scratch_on_current_device(void** out) {
 extern "C" gdn_status gdn_tree_verify_noalloc(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
                                               const void* x_raw, const float* conv_w, const void* beta,
                                               const void* log_g, float* state, float* conv_state, float* out_o,
-                                              float* boundary_states, gdn_banks* banks, cudaStream_t stream) {
+                                              float* boundary_states, gdn_banks* banks, int32_t flags,
+                                              cudaStream_t stream) {
   gdn::clear_error();
   if (!d || !sched) return gdn::fail(GDN_ERR_INVALID_ARG, "dims or schedule is NULL");
   if (layers < 1 || sched->B < 1 || sched->n_max < 1)
@@ -74,5 +75,5 @@ extern "C" gdn_status gdn_tree_verify_noalloc(const gdn_dims* d, int32_t layers,
   gdn_status st = scratch_on_current_device(&ws);
   if (st != GDN_OK) return st;
   return gdn_tree_verify(d, layers, sched, x_raw, conv_w, beta, log_g, state, conv_state, out_o, boundary_states,
-                         banks, ws, GDN_NOALLOC_SCRATCH_BYTES, stream);
+                         banks, ws, GDN_NOALLOC_SCRATCH_BYTES, flags, stream);
 }

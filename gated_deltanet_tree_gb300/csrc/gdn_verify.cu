@@ -8,9 +8,17 @@
 // on with the same live tile).
 //
 // Work unit: one CTA per (request, layer, v-head, column slice of d_v).  The CTA
-// walks every chain of its tree in schedule order (wave, head): the root chain
-// continues from the folded committed state; any other chain reloads the state
-// that a chain of an earlier wave of the same CTA stored at its boundary slot.
+// walks its whole tree depth first, light children before the heavy one, as the
+// packed schedule's ops list it: a heavy-light chain continues in registers from
+// head to tail; a branching node's state is materialised once and stashed, the
+// first child continues from the registers and each later child reloads the
+// stash.  Stashes live in tensor memory (tcgen05): the 32x32b access shape gives
+// every thread its own TMEM lane, so a register tile moves in and out without
+// crossing lanes, and the 256 KB per SM holds two levels of stash for each of
+// the four resident CTAs -- enough for every tree whose root paths cross at most
+// two light edges (all 22-node top-4 DDTrees here).  Deeper stashes spill to the
+// node's boundary slot in HBM, which is also where boundary states are written
+// when the caller asks for them.
 //
 // Thread layout: a thread owns RPT consecutive rows x 4 consecutive columns of
 // the [d_k][d_v] tile, held as packed (row r, row r+1) fp32 pairs so the tile
@@ -78,6 +86,49 @@ __device__ __forceinline__ u64 mul2(u64 a, u64 b) {
   return d;
 }
 
+// ---- tensor memory (tcgen05) as a stash for register tiles: the 32x32b access shape gives each
+// thread of a warp its own lane, so a tile held in registers moves in and out without crossing lanes.
+__host__ __device__ constexpr uint32_t tmem_columns(int words) {   // allocation: a power of two >= 32, or none
+  return words <= 0 ? 0u : words <= 32 ? 32u : words <= 64 ? 64u : words <= 128 ? 128u : words <= 256 ? 256u : 512u;
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The loaded registers are defined only after tcgen05.wait::ld: tie them to a point after the wait so
+// that no use is scheduled before it.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+               "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
 template <typename InT>
 __device__ __forceinline__ float load_in(const InT* p, size_t i);
 template <>
@@ -123,7 +174,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   constexpr int CG = CPB / kCols;          // column groups per CTA
   constexpr int NW = (DK / RPT) * CG / 32; // warps per CTA
   constexpr int cpb = CPB;
+  constexpr int kWords = 2 * kCols * NP;   // 32-bit words of a thread's tile = its tensor-memory columns per level
   static_assert(RPT % 4 == 0 && CG <= 32 && (DK / RPT) * CG % 32 == 0, "layout");
+  static_assert(kWords % 16 == 0 && (kCols * NP) % 8 == 0 && tmem_columns(kTmemLevels * kWords) <= 512, "stash");
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const Smem<DK> L{p.n_max, cpb};
@@ -234,20 +287,45 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   };
 
   float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
+
+  // ---- tensor memory first.  Until a CTA of a kernel that allocates tensor memory gives up its
+  // allocation permit, the SM holds back further CTAs of it; so warp 0 allocates the stash this tree's
+  // schedule asks for (`levels` copies of every thread's register tile: thread t of warp w owns lane
+  // 32 (w % 4) + t, a level is kWords consecutive columns) and relinquishes the permit at once.  The
+  // same warp releases the columns at the very end, after every warp's last access; the body below
+  // leaves only by uniform returns, so every thread reaches that point.
+  const SchedLayout lay{p.n_max};
+  const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
+  const int levels_rec = rec ? rec[4] : 0;
+  const int levels = (levels_rec >= 0 && levels_rec <= kTmemLevels) ? levels_rec : 0;
+  const uint32_t tcols = tmem_columns(levels * kWords);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L.bar0(nwarps) + 2);
+  if (warp == 0) {
+    __syncwarp();
+    if (tcols) tmem_alloc(tslot, tcols);
+    tmem_relinquish();
+  }
+  uint32_t tbase = 0;
+  if (tcols) {
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    tbase = *tslot;
+  }
+  const uint32_t tthread = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+  [&]() {
   load_tile(st);
 
   // ---- schedule header, pending length, staging barrier
-  if (launch_aborted(p.err)) return;   // an earlier CTA gave up on a wait
+  if (__syncthreads_or(launch_aborted(p.err))) return;   // an earlier CTA gave up on a wait
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar0(nwarps));
   if (tid == 0) mbar_init(bar);
-  const SchedLayout lay{p.n_max};
-  const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
-  int n = 0, n_chains = 0;
+  int n = 0;
   int32_t* srec = reinterpret_cast<int32_t*>(sm + L.rec0(nwarps));
   if (rec) {
     n = rec[0];
-    n_chains = rec[1];
-    if (n < 1 || n > p.n_max || n_chains < 1 || n_chains > n) {
+    if (n < 1 || n > p.n_max || levels_rec < 0 || levels_rec > kTmemLevels) {
       if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
       return;
     }
@@ -292,14 +370,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       }
     for (int i = tid; i < fn; i += blockDim.x)
       sm[L.fg() + i] = expf(p.pend_a[(nrow0 + (path[f0 + i] & kPathNodeMask)) * p.Hv + h]);
-    const bool ok = mbar_wait(bar, phase);
+    // one verdict for the whole CTA (this barrier also makes the plain-loaded scalars visible)
+    const bool ok = __syncthreads_and(mbar_wait(bar, phase));
     phase ^= 1;
     if (!ok) {
       if (tid == 0) device_error(p.err, GDN_DEVERR_TIMEOUT, b);
       mbar_wait(bar, phase ^ 1);   // let the copies land before the CTA exits
       return false;
     }
-    __syncthreads();   // plain-loaded scalars visible
     return true;
   };
 
@@ -338,20 +416,52 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   }
   __syncthreads();
 
+  const int32_t* parent = srec + lay.parent();
   const int32_t* bslot = srec + lay.bslot();
-  const int32_t* csrc = srec + lay.chain_src();
-  const int32_t* coff = srec + lay.chain_off();
-  const int32_t* cnodes = srec + lay.chain_nodes();
+  const int32_t* ops = srec + lay.ops();
   float* bnd_base = p.boundary + (static_cast<size_t>(bl) * p.nb_max * p.Hv + h) * tile +
                     static_cast<size_t>(row0) * p.dv + col;
   int parity = 0;
   const size_t slot_stride = static_cast<size_t>(p.Hv) * tile;
   const u64 zero2 = pack2(0.f, 0.f);
 
-  bool preloaded = false;        // the tile already holds this chain's source (loaded during the last leaf)
+  // ---- stash moves between the register tile and tensor memory
+  auto tmem_put = [&](int level) {
+    const uint32_t ta = tthread + static_cast<uint32_t>(level * kWords);
+    __syncwarp();   // the warp-collective tcgen05 accesses run converged
+#pragma unroll
+    for (int q = 0; q < kWords / 16; ++q) {
+      uint32_t r[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 f = unpack2(T[(q * 8 + e) / NP][(q * 8 + e) % NP]);
+        r[2 * e] = __float_as_uint(f.x);
+        r[2 * e + 1] = __float_as_uint(f.y);
+      }
+      tmem_st16(ta + 16 * q, r);
+    }
+    tmem_wait_st();
+  };
+  auto tmem_get = [&](int level) {
+    const uint32_t ta = tthread + static_cast<uint32_t>(level * kWords);
+    __syncwarp();
+    uint32_t r[kWords / 16][16];
+#pragma unroll
+    for (int q = 0; q < kWords / 16; ++q) tmem_ld16(ta + 16 * q, r[q]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < kWords / 16; ++q) {
+      reg_fence16(r[q]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        T[(q * 8 + e) / NP][(q * 8 + e) % NP] = pack2(__uint_as_float(r[q][2 * e]), __uint_as_float(r[q][2 * e + 1]));
+    }
+  };
+
+  bool preloaded = false;        // the tile already holds the next node's source (loaded during a leaf)
   // One node; the leaf flag and the "decay into the tile" flag are compile-time so each
   // combination is its own straight-line body (no predicated rare paths on common nodes).
-  auto step = [&](int node, int c, auto leaf_t, auto low_t) {
+  auto step = [&](int node, int pre, auto leaf_t, auto low_t) {
     constexpr bool kLeaf = decltype(leaf_t)::value;
     constexpr bool kLow = decltype(low_t)::value;
     const float* kvec = sm + L.kq(node);
@@ -374,16 +484,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         aq[cc] = fma2(T[cc][2 * j4 + 1], qq.y, aq[cc]);
       }
     }
-    // A chain ends at a leaf: its updated state is never read (leaves are not boundaries, and the
-    // fold rebuilds from the factor bank), so the tile is free after pass A -- start loading the
-    // next chain's source now, under this node's reduction.
+    // A leaf's updated state is never read (the fold rebuilds it from the factor bank), so the tile
+    // is free after pass A: when the next node reloads a stash from HBM, start that load now, under
+    // this node's reduction.
     if constexpr (kLeaf) {
-      if (c + 1 < n_chains) {
-        const int nsrc = csrc[c + 1];
-        if (nsrc >= 0 && nsrc < p.nb_max) {
-          load_tile(bnd_base + static_cast<size_t>(nsrc) * slot_stride);
-          preloaded = true;
-        }
+      if (pre >= 0) {
+        load_tile(bnd_base + static_cast<size_t>(pre) * slot_stride);
+        preloaded = true;
       }
     }
     float4 sk, sq;
@@ -457,44 +564,94 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
     }
     if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
-    const int slot = bslot[node];
-    if (slot >= p.nb_max || (kLeaf && slot >= 0)) {   // a boundary node has children: never a leaf
-      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-    } else if (slot >= 0) {
-      store_scaled(bnd_base + static_cast<size_t>(slot) * slot_stride, gam);
-    }
   };
   using kT = std::true_type;
   using kF = std::false_type;
 
-  for (int c = 0; c < n_chains; ++c) {
-    const int src = csrc[c];
-    const int i0 = coff[c], i1 = coff[c + 1];
-    if (src >= p.nb_max || i0 < 0 || i1 > n || i0 > i1) {
-      if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-      return;
+  // ---- the nodes in the schedule's depth-first order.  A node continues from the registers or
+  // reloads its parent's stash (tensor memory, or the parent's boundary slot in HBM); a node whose
+  // state is stashed is materialised first.  Every check below depends only on the schedule record,
+  // so the whole CTA takes the same branch.
+  bool bad = false;
+  for (int i = 0; i < n; ++i) {
+    const int op = ops[i];
+    const int node = op & kOpNode;
+    const int slot = node < n ? bslot[node] : -1;
+    if (node >= n || slot >= p.nb_max || ((op & kOpLeaf) && (op & kOpPush)) || ((op & kOpReload) && node == 0)) {
+      bad = true;
+      break;
     }
-    if (src >= 0) {
-      if (!preloaded) load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
+    if (op & kOpReload) {
+      if (!preloaded) {
+        if (op & kOpReloadGlobal) {
+          const int src = bslot[parent[node]];
+          if (src < 0 || src >= p.nb_max) {
+            bad = true;
+            break;
+          }
+          load_tile(bnd_base + static_cast<size_t>(src) * slot_stride);
+        } else {
+          const int lvl = (op >> kOpReloadLevelShift) & 3;
+          if (lvl >= levels) {
+            bad = true;
+            break;
+          }
+          tmem_get(lvl);
+        }
+      }
       gam = 1.f;
     }
     preloaded = false;
-    for (int i = i0; i < i1; ++i) {
-      const int node = cnodes[i];
-      if (node < 0 || node >= n) {
-        if (tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
-        return;
+    const bool low = gam * sm[L.g() + node] < kGammaFloor;
+    if (op & kOpLeaf) {
+      // the boundary slot the next node reloads from, if it does so from HBM: loaded during this leaf
+      int pre = -1;
+      if (i + 1 < n) {
+        const int nop = ops[i + 1];
+        const int nn = nop & kOpNode;
+        if ((nop & kOpReload) && (nop & kOpReloadGlobal) && nn > 0 && nn < n) {
+          const int nsrc = bslot[parent[nn]];
+          pre = nsrc < p.nb_max ? nsrc : -1;
+        }
       }
-      const bool low = gam * sm[L.g() + node] < kGammaFloor;
-      // the last node of a chain whose state nobody reads: a leaf (HLD chains always end at one; a
-      // schedule may also end a chain at a boundary node, whose state is stored)
-      if (i == i1 - 1 && bslot[node] < 0) {
-        if (low) step(node, c, kT{}, kT{});
-        else step(node, c, kT{}, kF{});
+      if (low) step(node, pre, kT{}, kT{});
+      else step(node, pre, kT{}, kF{});
+    } else {
+      if (low) step(node, -1, kF{}, kT{});
+      else step(node, -1, kF{}, kF{});
+    }
+    if (op & kOpPush) {
+      materialise(gam);
+      gam = 1.f;
+      if (op & kOpPushGlobal) {
+        if (slot < 0) {
+          bad = true;
+          break;
+        }
+        store_tile(bnd_base + static_cast<size_t>(slot) * slot_stride);
       } else {
-        if (low) step(node, c, kF{}, kT{});
-        else step(node, c, kF{}, kF{});
+        const int lvl = (op >> kOpPushLevelShift) & 3;
+        if (lvl >= levels) {
+          bad = true;
+          break;
+        }
+        tmem_put(lvl);
+        if (p.boundary_out && slot >= 0) store_tile(bnd_base + static_cast<size_t>(slot) * slot_stride);
       }
+    } else if (p.boundary_out && slot >= 0) {
+      store_scaled(bnd_base + static_cast<size_t>(slot) * slot_stride, gam);
+    }
+  }
+  if (bad && tid == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, b);
+  }();
+
+  if (tcols) {
+    tmem_fence_before();
+    __syncthreads();   // every warp's tensor-memory accesses are complete (each waited on its own)
+    tmem_fence_after();
+    if (warp == 0) {
+      __syncwarp();
+      tmem_dealloc(tbase, tcols);
     }
   }
 }

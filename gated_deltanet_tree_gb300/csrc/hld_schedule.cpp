@@ -142,8 +142,87 @@ extern "C" gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_sch
 
 extern "C" int32_t gdn_schedule_words(int32_t n_max) { return gdn::SchedLayout{n_max}.words(); }
 
-// Per-node-state schedule: no heavy edges, every node its own chain, every node with children
-// materialised; chains ordered by (depth, node).  Same packed layout as the heavy-light one.
+// The verify's walk of one tree: a depth-first order in which every node follows its parent, and
+// the stash traffic it implies.  Heavy-light (the SpecLA chains): children are visited light ones
+// first (ascending index), the heavy child last, so a chain continues in registers through every
+// node with one child.  A branching node's state is materialised and stashed once; its first child
+// continues from the registers, each later child reloads the stash, and the stash is released when
+// the last (heavy) child starts -- so at most (light edges on the root path) stashes are live, and
+// the first kTmemLevels of them sit in tensor memory, deeper ones in the node's boundary slot.
+// Per-node states (the comparison schedule): children by ascending index, every node with children
+// stashes its state in its boundary slot and every child reloads it from there.
+static void emit_ops(const int32_t* parent, int n, const int32_t* heavy, bool per_node,
+                     const std::vector<int32_t>& slot, int32_t* ops, int32_t* nflags, int* levels_used) {
+  std::vector<std::vector<int>> kids(n);
+  for (int i = 1; i < n; ++i) kids[parent[i]].push_back(i);
+  if (!per_node)
+    for (int v = 0; v < n; ++v) {
+      auto& k = kids[v];
+      for (size_t i = 0; i + 1 < k.size(); ++i)
+        if (k[i] == heavy[v]) std::swap(k[i], k[i + 1]);   // bubble the heavy child to the end
+    }
+  int next = 0, depth = 0, used = 0;
+  struct Frame { int v; size_t child; int32_t stash; bool pushed; };
+  std::vector<Frame> stack;
+  auto enter = [&](int v, int32_t src) {
+    int32_t op = v | src;
+    const auto& ch = kids[v];
+    int32_t stash = 0;
+    bool pushed = false;
+    if (ch.empty()) {
+      op |= gdn::kOpLeaf;
+    } else if (per_node || ch.size() >= 2) {
+      pushed = true;
+      if (per_node || depth >= gdn::kTmemLevels || slot[v] < 0) {
+        op |= gdn::kOpPush | gdn::kOpPushGlobal;
+        stash = gdn::kOpReload | gdn::kOpReloadGlobal;
+      } else {
+        op |= gdn::kOpPush | (depth << gdn::kOpPushLevelShift);
+        stash = gdn::kOpReload | (depth << gdn::kOpReloadLevelShift);
+        used = depth + 1 > used ? depth + 1 : used;
+      }
+      ++depth;
+    }
+    ops[next++] = op;
+    nflags[v] = pushed ? gdn::kNodeMaterialised : 0;
+    stack.push_back({v, 0, stash, pushed});
+  };
+  enter(0, 0);
+  while (!stack.empty()) {
+    Frame& f = stack.back();
+    const auto& ch = kids[f.v];
+    if (f.child == ch.size()) {
+      stack.pop_back();
+      continue;
+    }
+    const size_t i = f.child++;
+    const bool last = f.child == ch.size();
+    const int32_t src = (i == 0 && !per_node) ? 0 : f.stash;
+    if (f.pushed && last) --depth;   // the last child takes the stash over; its level is free again
+    enter(ch[i], src);               // may reallocate the stack: f is not used after this
+  }
+  *levels_used = used;
+}
+
+// One packed record (layout in gdn_tree.h).
+static void write_record(const int32_t* parent, int n, const gdn::SchedLayout& lay, int n_chains, int n_boundary,
+                         int n_waves, const std::vector<int32_t>& slot, const int32_t* heavy, bool per_node,
+                         int32_t* w) {
+  for (int i = 0; i < lay.words(); ++i) w[i] = -1;
+  w[0] = n;
+  w[1] = n_chains;
+  w[2] = n_boundary;
+  w[3] = n_waves;
+  for (int i = 0; i < n; ++i) {
+    w[lay.parent() + i] = parent[i];
+    w[lay.bslot() + i] = slot[i];
+  }
+  int levels = 0;
+  emit_ops(parent, n, heavy, per_node, slot, w + lay.ops(), w + lay.nflags(), &levels);
+  w[4] = levels;
+}
+
+// Per-node-state schedule: every node with children gets a boundary slot (ascending node order).
 static gdn_status pack_per_node(const int32_t* parent, int n, const gdn::SchedLayout& lay, int32_t* w,
                                 int* nb_out) {
   if (n < 1 || parent[0] != -1) return fail(GDN_ERR_INVALID_TREE, "parent[0] must be -1");
@@ -155,30 +234,11 @@ static gdn_status pack_per_node(const int32_t* parent, int n, const gdn::SchedLa
   }
   int max_depth = 0;
   for (int i = 0; i < n; ++i) max_depth = depth[i] > max_depth ? depth[i] : max_depth;
-  std::vector<int32_t> order;
-  for (int d = 0; d <= max_depth; ++d)
-    for (int i = 0; i < n; ++i)
-      if (depth[i] == d) order.push_back(i);
   std::vector<int32_t> slot(n, -1);
   int nb = 0;
   for (int i = 0; i < n; ++i)
     if (kids[i] > 0) slot[i] = nb++;
-  for (int i = 0; i < lay.words(); ++i) w[i] = -1;
-  w[0] = n;
-  w[1] = n;
-  w[2] = nb;
-  w[3] = max_depth + 1;
-  for (int i = 0; i < n; ++i) {
-    w[lay.parent() + i] = parent[i];
-    w[lay.bslot() + i] = slot[i];
-  }
-  for (int c = 0; c < n; ++c) {
-    const int v = order[c];
-    w[lay.chain_src() + c] = v == 0 ? -1 : slot[parent[v]];
-    w[lay.chain_off() + c] = c;
-    w[lay.chain_nodes() + c] = v;
-  }
-  w[lay.chain_off() + n] = n;
+  write_record(parent, n, lay, n, nb, max_depth + 1, slot, nullptr, true, w);
   *nb_out = nb;
   return GDN_OK;
 }
@@ -220,20 +280,8 @@ extern "C" gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* 
       return fail(GDN_ERR_INVALID_TREE, "request %d: n = %d outside 1..n_max (%d)", b, n[b], n_max);
     gdn_status st = build(parents + static_cast<size_t>(b) * n_max, n[b], h);
     if (st != GDN_OK) return fail(st, "request %d: %s", b, gdn_last_error());
-    int32_t* w = words + static_cast<size_t>(b) * lay.words();
-    for (int i = 0; i < lay.words(); ++i) w[i] = -1;
-    w[0] = h.n;
-    w[1] = h.n_chains;
-    w[2] = h.n_boundary;
-    w[3] = h.n_waves;
-    for (int i = 0; i < h.n; ++i) {
-      w[lay.parent() + i] = parents[static_cast<size_t>(b) * n_max + i];
-      w[lay.bslot() + i] = h.bslot[i];
-      w[lay.chain_nodes() + i] = h.chain_nodes[i];
-      w[lay.heavy() + i] = h.heavy[i];
-    }
-    for (int c = 0; c < h.n_chains; ++c) w[lay.chain_src() + c] = h.chain_src[c];
-    for (int c = 0; c <= h.n_chains; ++c) w[lay.chain_off() + c] = h.chain_off[c];
+    write_record(parents + static_cast<size_t>(b) * n_max, h.n, lay, h.n_chains, h.n_boundary, h.n_waves, h.bslot,
+                 h.heavy.data(), false, words + static_cast<size_t>(b) * lay.words());
     if (h.n_boundary > nb_max) nb_max = h.n_boundary;
   }
   if (nb_max_out) *nb_max_out = nb_max;

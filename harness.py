@@ -108,10 +108,10 @@ class GpuSession:
             self.path_t[step] = paths_tensor(self.plan.paths[step], self.w.n_max, self.device)
         return self.path_t[step]
 
-    def verify(self, step: int, stream=None):
+    def verify(self, step: int, stream=None, boundary_scratch: bool = False):
         X, BE, AG = self.step_inputs(step)
         self.ver.verify(self.schedule(step), X, self.conv_w, BE, AG, self.state, self.conv_state, self.out_o,
-                        self.boundary, stream)
+                        self.boundary, stream, boundary_scratch)
 
     def local_layer(self, l: int) -> int:
         return self.layer_ids.index(l)

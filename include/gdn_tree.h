@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 #define GDN_MAX_NODES 64   /* largest tree (n_max) the kernels accept */
 #define GDN_MAX_TAPS 8     /* largest conv kernel K */
 
@@ -113,14 +113,29 @@ gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_schedule* out)
 
 /* ---------------------------------------------------------------------------
  * Packed batch schedule: the compact form the kernels read.
- * One record of gdn_schedule_words(n_max) int32 per request:
+ * One record of gdn_schedule_words(n_max) = 5 + 4 n_max int32 per request:
  *   [0] n  [1] n_chains  [2] n_boundary  [3] n_waves
- *   [4 .. 4+n_max)              parent (unused entries -1)
- *   [4+n_max .. 4+2n_max)       boundary slot of each node (-1: none)
- *   [4+2n_max .. 4+3n_max)      source slot of each chain in schedule order
- *   [4+3n_max .. 5+4n_max)      chain offsets into the node list
- *   [5+4n_max .. 5+5n_max)      nodes of the chains, concatenated
- *   [5+5n_max .. 5+6n_max)      heavy child of each node (-1: leaf)
+ *   [4] stash levels the verify keeps in tensor memory (0..2)
+ *   [5 .. 5+n_max)              parent (unused entries -1)
+ *   [5+n_max .. 5+2n_max)       boundary slot of each node (-1: none)
+ *   [5+2n_max .. 5+3n_max)      node flags: bit 0 = the state after the node is
+ *                               materialised and stashed (its children start from it)
+ *   [5+3n_max .. 5+4n_max)      verify ops, one per node in walk order:
+ *       bits 0-7   node
+ *       bit 8      reload: start from the parent's stash (else continue from the
+ *                  previous node's registers -- the previous node is the parent)
+ *       bit 9      the stash is the parent's boundary slot in boundary_states
+ *                  (else tensor memory, level in bits 10-11)
+ *       bit 12     push: after the node, materialise the state and stash it
+ *       bit 13     in the node's boundary slot (else tensor memory, level in bits 14-15)
+ *       bit 16     leaf: the node has no children
+ * Heavy-light walk (SpecLA article, "链分解与依赖波 HLD 调度"): depth first, light
+ * children before the heavy child, so every chain runs in registers from head to
+ * tail.  A branching node (two or more children = a boundary node) is stashed
+ * once; its first child continues from the registers, the others reload the
+ * stash, the last (heavy) one releases it.  At most (light edges on a root path)
+ * stashes are live; the first two levels sit in tensor memory on the SM, deeper
+ * ones spill to the node's boundary slot.
  * gdn_pack_schedules runs gdn_hld_schedule on every request's tree and writes
  * the records into words_host (B * gdn_schedule_words(n_max) int32, caller-
  * owned host memory); *nb_max_out receives the largest boundary count.  The
@@ -131,14 +146,48 @@ int32_t gdn_schedule_words(int32_t n_max);
 gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
                               int32_t* words_host, int32_t* nb_max_out);
 
-/* Per-node-state schedule in the same packed layout, for comparison with the heavy-light one: no heavy
- * edges, every node its own chain (ordered by depth, then node), every node with children materialised
- * in a boundary slot.  The verify then reloads and stores a state at every step of the tree -- the
- * rollback-by-snapshot scheme the SpecLA article replaces ("状态驻留验证": state traffic twice per
- * token instead of twice per chain).  Same arguments and results as gdn_pack_schedules; nb_max is the
- * number of nodes with children. */
+/* Per-node-state schedule in the same packed layout, for comparison with the heavy-light one: every node
+ * with children stashes its state in its boundary slot (in HBM) and every child reloads it from there -- the
+ * rollback-by-snapshot scheme the SpecLA article replaces ("状态驻留验证": state traffic twice per token
+ * instead of twice per chain).  The walk is depth first, children by index.  Same arguments and results as
+ * gdn_pack_schedules; nb_max is the number of nodes with children. */
 gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
                                        int32_t* words_host, int32_t* nb_max_out);
+
+/* ---------------------------------------------------------------------------
+ * DDTree construction with confidence pruning (host, pure).
+ * Luce DFlash README, "How it works": a best-first tree of up to `budget`
+ * nodes spans the draft's top-K branches at each position (flags
+ * --ddtree-budget, default 22, and --ddtree-tau, a confidence margin that
+ * SpecLA sets to 6); SpecLA article, section "一键开启": nodes scoring below
+ * q* - tau are pruned; section "正确性如何保证": cumulative-score pruning,
+ * ancestor closure, budget cap.
+ *
+ * logp: host, [depth_max][top_k] fp32, row d-1 = the draft's log-probabilities
+ *   of its top_k tokens at depth d (every entry <= 0 and not NaN, else
+ *   GDN_ERR_INVALID_ARG).  A node is a sequence of ranks; score = cumulative
+ *   log-probability from the root (double); the root scores 0.
+ * budget: 1..GDN_MAX_NODES nodes, root included.
+ * tau: >= 0 prunes every node with score < q* - tau, q* = the best candidate
+ *   score (= max_r logp[0][r]); tau < 0 disables pruning; NaN is an error.
+ * flags: GDN_DDTREE_CHAIN_SEED inserts the greedy chain (best rank at every
+ *   depth, ties to the lower rank) first, as far as it is eligible and fits.
+ * The remaining nodes are the best eligible candidates in the order (higher
+ * score, lower depth, lexicographically smaller rank sequence), added while
+ * the budget allows.  Output (caller-owned, >= budget entries each; depth,
+ * rank and score may be NULL), numbered in DFS preorder with children by
+ * rank, so parent[0] = -1 and parent[i] < i: parent, depth, rank (root -1),
+ * score; *n_out = the node count.  The tree feeds gdn_hld_schedule /
+ * gdn_pack_schedules as it is.
+ * gdn_ddtree_build_batch builds B trees from logp [B][depth_max][top_k] into
+ * parents [B][n_max] (n_max >= budget, unused entries -1) and n [B].
+ * ------------------------------------------------------------------------- */
+#define GDN_DDTREE_CHAIN_SEED 1
+gdn_status gdn_ddtree_build(const float* logp, int32_t depth_max, int32_t top_k, int32_t budget, double tau,
+                            int32_t flags, int32_t* parent, int32_t* depth, int32_t* rank, double* score,
+                            int32_t* n_out);
+gdn_status gdn_ddtree_build_batch(const float* logp, int32_t B, int32_t depth_max, int32_t top_k, int32_t budget,
+                                  double tau, int32_t flags, int32_t n_max, int32_t* parents, int32_t* n);
 
 typedef struct {
   int32_t B;               /* requests */
@@ -160,7 +209,8 @@ typedef struct {
  *                                           only read/written in conv_mode 1, may be NULL otherwise)
  *   pend_path [B][n_max] int32, pend_len [B] int32: the accepted path recorded by
  *   gdn_commit_fold -- node index in the low 16 bits, bit 30 set where the path
- *   enters a light child (a chain head); err [4] int32, zeroed by the caller
+ *   enters a node whose parent's state the verify materialised (node flags bit 0
+ *   of the parent); err [4] int32, zeroed by the caller
  *   before first use.
  * Host fields (set by gdn_banks_init, then advanced by the calls):
  *   write_bank: bank the next verify writes; pend_bank: bank holding the
@@ -185,6 +235,8 @@ gdn_status gdn_banks_init(gdn_banks* banks, int32_t B, int32_t layers, int32_t n
  * every node, fp32.  Pass a device buffer of at least this size. */
 size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t n_max);
 
+#define GDN_VERIFY_BOUNDARY_SCRATCH 1   /* boundary_states is scratch, not output */
+
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify -- fold the pending path, then verify a batch of trees.
  * SpecLA article, "延迟融合提交" and "状态驻留验证".
@@ -193,8 +245,9 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  * folded into each head's state tile as it is loaded -- T <- exp(a_t) T + k_t u_t^T
  * along the path, and the conv window takes the path's last K-1 raw rows -- and
  * the committed state and conv window are written back once.  Every node of
- * every tree is then advanced from its parent's state; each chain of the
- * heavy-light schedule keeps its tile on chip from head to tail.
+ * every tree is then advanced from its parent's state, in the walk order of the
+ * packed ops: each chain of the heavy-light schedule keeps its tile in
+ * registers from head to tail, and branch states wait in tensor memory.
  *
  *   x_raw      [B][layers][n_max][C]       in_dtype (bf16 or fp32)
  *   conv_w     [layers][C][K]              fp32 (conv_mode 1; else may be NULL)
@@ -205,6 +258,10 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *   out_o      [B][layers][n_max][Hv][dv]  fp32 out: o of every node
  *   boundary_states [B][layers][nb_max][Hv][dk][dv] fp32 out: the state after each
  *              boundary node, by slot.  May be NULL only if no tree has a boundary.
+ *              With GDN_VERIFY_BOUNDARY_SCRATCH in flags it is scratch instead: only
+ *              stashes that spill out of tensor memory are written there, and its
+ *              contents are unspecified on return.
+ *   flags      0 or GDN_VERIFY_BOUNDARY_SCRATCH (other bits: GDN_ERR_INVALID_ARG)
  *   banks      factors of every node are written into bank write_bank
  *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
  * Rows of nodes >= n[b] are neither read nor written.
@@ -212,7 +269,8 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
 gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
                            const void* x_raw, const float* conv_w, const void* beta, const void* log_g,
                            float* state, float* conv_state, float* out_o, float* boundary_states,
-                           gdn_banks* banks, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                           gdn_banks* banks, void* workspace, size_t workspace_bytes, int32_t flags,
+                           cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify_noalloc -- gdn_tree_verify without a workspace argument, for
@@ -237,7 +295,7 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
 gdn_status gdn_tree_verify_noalloc(const gdn_dims* d, int32_t layers, const gdn_batch_schedule* sched,
                                    const void* x_raw, const float* conv_w, const void* beta, const void* log_g,
                                    float* state, float* conv_state, float* out_o, float* boundary_states,
-                                   gdn_banks* banks, cudaStream_t stream);
+                                   gdn_banks* banks, int32_t flags, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gdn_commit_fold -- record the accepted path of the last verify as pending.

@@ -39,7 +39,8 @@ def test_exports_every_declared_function(N):
     lib = ctypes.CDLL(N.LIB_PATH)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in gdn_tree.h but not exported"
-    assert N.gdn_abi_version() == 1
+    version = re.search(r"#define GDN_ABI_VERSION (\d+)", open(os.path.join(ROOT, "include", "gdn_tree.h")).read())
+    assert N.gdn_abi_version() == int(version.group(1))
 
 
 def _compare(N, parent):
@@ -74,29 +75,101 @@ def test_invalid_trees_rejected(N):
         N.gdn_hld_schedule(np.zeros(0, dtype=np.int32))
 
 
+RELOAD, RELOAD_GLOBAL, PUSH, PUSH_GLOBAL, LEAF = 1 << 8, 1 << 9, 1 << 12, 1 << 13, 1 << 16
+
+
+def walk_order(parent, heavy_last):
+    """Depth-first preorder; children by index, or light ones by index and the heavy child last."""
+    m = len(parent)
+    kids = [[] for _ in range(m)]
+    for v in range(1, m):
+        kids[parent[v]].append(v)
+    if heavy_last:
+        heavy = O.hld_schedule(list(parent))["heavy"]
+        kids = [[c for c in k if c != heavy[v]] + ([heavy[v]] if heavy[v] >= 0 else []) for v, k in enumerate(kids)]
+    order, stack = [], [0]
+    while stack:
+        v = stack.pop()
+        order.append(v)
+        stack.extend(reversed(kids[v]))
+    return order, kids
+
+
+def simulate_walk(parent, w, n_max):
+    """Run the verify's walk over the ops with abstract registers and stashes; every node must start
+    from its parent's state.  Returns (ops, levels, nodes pushed to HBM, nodes reloaded)."""
+    m = len(parent)
+    bslot = list(w[5 + n_max:5 + n_max + m])
+    nflags = list(w[5 + 2 * n_max:5 + 2 * n_max + m])
+    ops = [int(x) for x in w[5 + 3 * n_max:5 + 3 * n_max + m]]
+    levels = int(w[4])
+    assert 0 <= levels <= 2
+    kids = np.bincount(np.asarray(parent[1:], dtype=np.int64), minlength=m) if m > 1 else np.zeros(1, int)
+    reg, tmem, glob = None, {}, {}
+    pushed_global, reloaded, used = [], [], -1
+    for i, op in enumerate(ops):
+        v = op & 0xFF
+        if op & RELOAD:
+            assert v != 0
+            if op & RELOAD_GLOBAL:
+                src = glob.get(bslot[parent[v]])
+            else:
+                lvl = (op >> 10) & 3
+                assert lvl < levels
+                src = tmem.get(lvl)
+            assert src == parent[v], (i, v)
+            reloaded.append(v)
+        else:
+            assert (i == 0 and v == 0) or reg == parent[v], (i, v)
+        leaf = bool(op & LEAF)
+        assert leaf == (kids[v] == 0)
+        reg = None if leaf else v
+        assert bool(op & PUSH) == bool(nflags[v] & 1)
+        if op & PUSH:
+            assert not leaf
+            if op & PUSH_GLOBAL:
+                assert bslot[v] >= 0
+                glob[bslot[v]] = v
+                pushed_global.append(v)
+            else:
+                lvl = (op >> 14) & 3
+                assert lvl < levels
+                tmem[lvl] = v
+                used = max(used, lvl)
+    assert levels == used + 1
+    return ops, pushed_global, reloaded
+
+
 def test_packed_layout(N):
     rng = np.random.default_rng(3)
     n_max = 24
-    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(6)] + [S.ddtree(22, 4, 10, rng)]
+    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(40)] + \
+            [S.ddtree(22, 4, 10, rng) for _ in range(10)] + [S.chain_tree(n_max)]
     P = np.full((len(trees), n_max), -1, dtype=np.int32)
     n = np.array([len(t) for t in trees], dtype=np.int32)
     for b, t in enumerate(trees):
         P[b, :len(t)] = t
     words, nb_max = N.gdn_pack_schedules(P, n)
-    assert words.shape == (len(trees), 5 + 6 * n_max)
+    assert words.shape == (len(trees), 5 + 4 * n_max)
     assert nb_max == max(O.hld_schedule(list(t))["n_boundary"] for t in trees)
     for b, t in enumerate(trees):
         s = O.hld_schedule(list(t))
         w = words[b]
         m = len(t)
         assert list(w[:4]) == [m, s["n_chains"], s["n_boundary"], s["n_waves"]]
-        assert list(w[4:4 + m]) == list(t)
-        assert list(w[4 + n_max:4 + n_max + m]) == s["boundary_slot"]
-        nc = s["n_chains"]
-        assert list(w[4 + 2 * n_max:4 + 2 * n_max + nc]) == s["chain_src_slot"]
-        assert list(w[4 + 3 * n_max:5 + 3 * n_max + nc]) == s["chain_off"]
-        assert list(w[5 + 4 * n_max:5 + 4 * n_max + m]) == s["chain_nodes"]
-        assert list(w[5 + 5 * n_max:5 + 5 * n_max + m]) == s["heavy"]
+        assert list(w[5:5 + m]) == list(t)
+        assert list(w[5 + n_max:5 + n_max + m]) == s["boundary_slot"]
+        ops, pushed_global, reloaded = simulate_walk(list(t), w, n_max)
+        order, kids = walk_order(list(t), heavy_last=True)
+        assert [op & 0xFF for op in ops] == order
+        # chains stay in registers: only the later children of a branching node reload
+        assert sorted(reloaded) == sorted(c for v in range(m) if len(kids[v]) >= 2 for c in kids[v][1:])
+        # stashed = the boundary nodes; those at a stash depth of two or more spill to HBM
+        assert sorted(v for v in range(m) if w[5 + 2 * n_max + v] & 1) == s["boundary_node"]
+        light_depth = [0] * m
+        for v in range(1, m):
+            light_depth[v] = light_depth[t[v]] + (1 if s["heavy"][t[v]] != v else 0)
+        assert sorted(pushed_global) == [v for v in s["boundary_node"] if light_depth[v] >= 2]
     with pytest.raises(N.GdnError) as e:
         N.gdn_pack_schedules(np.full((1, 65), -1, dtype=np.int32), np.array([3], dtype=np.int32))
     assert e.value.status == N.GDN_ERR_UNSUPPORTED
@@ -195,7 +268,7 @@ def test_workspace_bytes(N):
 def test_per_node_schedule_layout(N):
     rng = np.random.default_rng(9)
     n_max = 20
-    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(8)] + [S.chain_tree(n_max)]
+    trees = [S.random_tree(int(rng.integers(1, n_max + 1)), rng) for _ in range(30)] + [S.chain_tree(n_max)]
     P = np.full((len(trees), n_max), -1, dtype=np.int32)
     n = np.array([len(t) for t in trees], dtype=np.int32)
     for b, t in enumerate(trees):
@@ -205,15 +278,11 @@ def test_per_node_schedule_layout(N):
         m, w = len(t), words[b]
         kids = np.bincount(t[1:], minlength=m) if m > 1 else np.zeros(1, dtype=int)
         internal = [v for v in range(m) if kids[v] > 0]
-        assert list(w[:3]) == [m, m, len(internal)]
-        bslot = list(w[4 + n_max:4 + n_max + m])
+        assert list(w[:3]) == [m, m, len(internal)] and w[4] == 0
+        bslot = list(w[5 + n_max:5 + n_max + m])
         assert [v for v in range(m) if bslot[v] >= 0] == internal
-        order = list(w[5 + 4 * n_max:5 + 4 * n_max + m])
-        depth = [len(O.root_path(t, v)) - 1 for v in range(m)]
-        assert order == sorted(range(m), key=lambda v: (depth[v], v))
-        src = list(w[4 + 2 * n_max:4 + 2 * n_max + m])
-        for c, v in enumerate(order):
-            assert src[c] == (-1 if v == 0 else bslot[t[v]])
-        assert list(w[4 + 3 * n_max:5 + 3 * n_max + m]) == list(range(m + 1))
-        assert all(x == -1 for x in w[5 + 5 * n_max:5 + 5 * n_max + m])     # no heavy edges
+        ops, pushed_global, reloaded = simulate_walk(list(t), w, n_max)
+        assert [op & 0xFF for op in ops] == walk_order(list(t), heavy_last=False)[0]
+        assert sorted(pushed_global) == internal          # every state with children goes to HBM ...
+        assert sorted(reloaded) == list(range(1, m))      # ... and every child reloads it
     assert nb_max == max(int((np.bincount(t[1:], minlength=len(t)) > 0).sum()) if len(t) > 1 else 0 for t in trees)

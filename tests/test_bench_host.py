@@ -64,3 +64,29 @@ def test_algorithmic_bytes_by_hand():
     expect += 2 * (32 + 32 + 1) * 4                      # pending k, u, a
     expect += C * 4 * 4                                  # conv weights
     assert bench.algorithmic_bytes(w, [3], [1], [2]) == expect
+
+
+def test_algorithmic_fma_by_hand():
+    # 2 requests, 1 layer, Hv=2, d=4: n=3 with 2 leaves and L=1; n=1 (a leaf) and L=0
+    w = S.workload(1).replace(B=2, layers=1, Hk=1, Hv=2, dk=4, dv=4)
+    per_elem = (2 * 3 + (3 - 2) + 1) + (2 * 1 + 0 + 0)
+    assert bench.algorithmic_fma(w, [3, 1], [2, 1], [1, 0]) == per_elem * 2 * 4 * 4
+    assert abs(bench.fp32_peak_tflops(152, 2070.0) - 80.55) < 0.01
+
+
+def test_hbm_stashes_counts_spilled_pushes():
+    # a perfect binary tree of 15 nodes: the third stash level (light depth two) spills to HBM
+    from gated_deltanet_tree_gb300.build import build
+    build()
+    from gated_deltanet_tree_gb300 import _native as N
+    parent = np.array([-1] + [(i - 1) // 2 for i in range(1, 15)], dtype=np.int32)
+    n_max = 16
+    P = np.full((1, n_max), -1, dtype=np.int32)
+    P[0, :len(parent)] = parent
+    words, _ = N.gdn_pack_schedules(P, np.array([len(parent)], dtype=np.int32))
+    ops = words[0, 5 + 3 * n_max:5 + 3 * n_max + len(parent)]
+    spilled = int((((ops >> 12) & 3) == 3).sum())
+    assert spilled >= 1 and words[0, 4] == 2
+    assert bench.hbm_stashes(words, n_max) == [spilled]
+    assert bench.hbm_stashes(N.gdn_pack_schedules_per_node(P, np.array([len(parent)], dtype=np.int32))[0],
+                             n_max) == [int((np.bincount(parent[1:], minlength=len(parent)) > 0).sum())]

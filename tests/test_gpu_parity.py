@@ -139,6 +139,56 @@ def test_per_node_state_schedule(cfg):
     run_parity(w, plan=plan)
 
 
+def binary_tree(n):
+    return np.array([-1] + [(i - 1) // 2 for i in range(1, n)], dtype=np.int32)
+
+
+@pytest.mark.parametrize("cfg", [1, 2], ids=["tiny", "qwen"])
+def test_deep_light_depth_spills_stashes_to_hbm(cfg):
+    # perfect binary trees (light depth 4 at 31 nodes) and random 32-node trees: stashes two or more
+    # levels deep leave tensor memory for the boundary slots, and every node must still match
+    from harness import WorkloadPlan
+    n_max = 32
+    w = S.workload(cfg).replace(B=3, layers=2 if cfg == 1 else 1, n_max=n_max, budget=n_max, path_max=n_max,
+                                steps=3, tree="random")
+    rng = np.random.default_rng(17)
+    trees, paths = [], []
+    for s in range(w.steps):
+        ts = [binary_tree(31), binary_tree(n_max), S.random_tree(n_max, rng)]
+        trees.append(ts)
+        paths.append([S.random_walk_path(t, rng, max_len=n_max) for t in ts])
+    run_parity(w, plan=WorkloadPlan(w, trees, paths))
+
+
+def test_boundary_scratch_changes_no_result():
+    # with boundary states as scratch the outputs, banks and committed states are bit-identical
+    from harness import GpuSession, WorkloadPlan
+    n_max = 32
+    w = S.workload(2).replace(B=3, layers=2, n_max=n_max, budget=n_max, path_max=n_max, steps=3, tree="random")
+    rng = np.random.default_rng(23)
+    trees = [[binary_tree(31), S.ddtree(22, 4, 10, rng), S.random_tree(n_max, rng)] for _ in range(w.steps)]
+    paths = [[S.random_walk_path(t, rng, max_len=n_max) for t in ts] for ts in trees]
+    plan = WorkloadPlan(w, trees, paths)
+    a, b = GpuSession(w, plan), GpuSession(w, plan)
+    for s in range(w.steps):
+        a.verify(s)
+        b.verify(s, boundary_scratch=True)
+        torch.cuda.synchronize()
+        assert torch.equal(a.out_o, b.out_o), s
+        assert torch.equal(a.state, b.state), s
+        for f in ("k", "u", "a", "x"):
+            assert torch.equal(a.ver.bank_view(f, a.ver.banks.verified_bank),
+                               b.ver.bank_view(f, b.ver.banks.verified_bank)), (s, f)
+        a.commit(s)
+        b.commit(s)
+    a.finish()
+    b.finish()
+    torch.cuda.synchronize()
+    assert torch.equal(a.state, b.state)
+    a.ver.check_error()
+    b.ver.check_error()
+
+
 def test_qwen_like_single_layer():
     w = S.workload(2).replace(steps=3)
     run_parity(w)
