@@ -146,11 +146,9 @@ struct Smem {
   int n_max, cpb;
   __device__ int kq(int node) const { return node * 2 * DK; }                  // [n_max][2][DK]
   __device__ int v(int node) const { return n_max * 2 * DK + node * cpb; }     // [n_max][cpb]
-  __device__ int g() const { return n_max * (2 * DK + cpb); }                  // [n_max] each
-  __device__ int beta() const { return g() + n_max; }
-  __device__ int a() const { return beta() + n_max; }
-  __device__ int kqdot() const { return a() + n_max; }
-  __device__ int fold0() const { return (kqdot() + n_max + 3) & ~3; }
+  // per node one float4: (g = exp(a), beta, k . q, a)
+  __device__ int sc(int node) const { return n_max * (2 * DK + cpb) + 4 * node; }
+  __device__ int fold0() const { return sc(n_max); }
   __device__ int fk(int i) const { return fold0() + i * DK; }                   // [kFoldChunk][DK]
   __device__ int fu(int i) const { return fold0() + kFoldChunk * DK + i * cpb; } // [kFoldChunk][cpb]
   __device__ int fg() const { return fold0() + kFoldChunk * (DK + cpb); }      // [kFoldChunk]
@@ -161,7 +159,7 @@ struct Smem {
 
 template <int DK>
 size_t smem_bytes(int n_max, int cpb, int warps) {
-  const int fold0 = (n_max * (2 * DK + cpb) + 4 * n_max + 3) & ~3;
+  const int fold0 = n_max * (2 * DK + cpb) + 4 * n_max;
   const int part0 = (fold0 + kFoldChunk * (DK + cpb) + kFoldChunk + 3) & ~3;
   const int words = SchedLayout{n_max}.words();
   const int bar0 = (part0 + 2 * warps * 2 * cpb + words + 3) & ~3;
@@ -269,7 +267,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       materialise(gam1);
       gam1 = 1.f;
     }
-    const float r = __frcp_rn(gam1);
+    const float r = __fdividef(1.f, gam1);
     update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
     return gam1;
   };
@@ -364,9 +362,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
     if (tree)
       for (int node = tid; node < n; node += blockDim.x) {
         const float a = load_in<InT>(logg, (nrow0 + node) * p.Hv + h);
-        sm[L.a() + node] = a;
-        sm[L.g() + node] = expf(a);
-        sm[L.beta() + node] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
+        sm[L.sc(node) + 0] = expf(a);
+        sm[L.sc(node) + 1] = load_in<InT>(beta, (nrow0 + node) * p.Hv + h);
+        sm[L.sc(node) + 3] = a;
+        if (s == 0) p.a_out[(nrow0 + node) * p.Hv + h] = a;   // the bank's log-gate, exact
       }
     for (int i = tid; i < fn; i += blockDim.x)
       sm[L.fg() + i] = expf(p.pend_a[(nrow0 + (path[f0 + i] & kPathNodeMask)) * p.Hv + h]);
@@ -412,7 +411,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
     for (int e = lane; e < DK; e += 32) acc = fmaf(kk[e], kk[DK + e], acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) sm[L.kqdot() + node] = acc;
+    if (lane == 0) sm[L.sc(node) + 2] = acc;
   }
   __syncthreads();
 
@@ -459,9 +458,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   };
 
   bool preloaded = false;        // the tile already holds the next node's source (loaded during a leaf)
+  const size_t node_stride = static_cast<size_t>(p.Hv) * p.dv;          // o and u rows of consecutive nodes
+  float* o_base = p.out_o + (nrow0 * p.Hv + h) * p.dv + col;
+  float* u_base = p.u_out + (nrow0 * p.Hv + h) * p.dv + col;
   // One node; the leaf flag and the "decay into the tile" flag are compile-time so each
   // combination is its own straight-line body (no predicated rare paths on common nodes).
-  auto step = [&](int node, int pre, auto leaf_t, auto low_t) {
+  auto step = [&](int node, int pre, float g, float4 nsc, auto leaf_t, auto low_t) {
     constexpr bool kLeaf = decltype(leaf_t)::value;
     constexpr bool kLow = decltype(low_t)::value;
     const float* kvec = sm + L.kq(node);
@@ -512,12 +514,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       sq.z += __shfl_xor_sync(0xffffffffu, sq.z, m);
       sq.w += __shfl_xor_sync(0xffffffffu, sq.w, m);
     }
-    // warps: partials [parity][warp][k|q][cpb]
+    // warps: partials [parity][warp][k|q][cpb]; the row groups of a warp hold equal sums after the
+    // butterfly, so every lane stores (same value, same address) and the warp does not diverge
     float* part = sm + L.part0() + parity * (nwarps * 2 * cpb);
-    if (lane < CG) {
-      *reinterpret_cast<float4*>(part + (warp * 2 + 0) * cpb + c0) = sk;
-      *reinterpret_cast<float4*>(part + (warp * 2 + 1) * cpb + c0) = sq;
-    }
+    *reinterpret_cast<float4*>(part + (warp * 2 + 0) * cpb + c0) = sk;
+    *reinterpret_cast<float4*>(part + (warp * 2 + 1) * cpb + c0) = sq;
     __syncthreads();
     sk = *reinterpret_cast<const float4*>(part + c0);
 #pragma unroll
@@ -526,15 +527,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       sk.x += t.x; sk.y += t.y; sk.z += t.z; sk.w += t.w;
     }
     parity ^= 1;
-    const float g = gam * sm[L.g() + node];   // gamma' of this node
-    const float bt = sm[L.beta() + node];
+    const float bt = nsc.y;
     const float4 v = *reinterpret_cast<const float4*>(sm + L.v(node) + c0);
     float4 u;
     u.x = bt * (v.x - g * sk.x);
     u.y = bt * (v.y - g * sk.y);
     u.z = bt * (v.z - g * sk.z);
     u.w = bt * (v.w - g * sk.w);
-    const size_t row = nrow0 + node;
     if (rg == 0) {
       sq = *reinterpret_cast<const float4*>(part + cpb + c0);
 #pragma unroll
@@ -542,14 +541,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         const float4 t = *reinterpret_cast<const float4*>(part + (w * 2 + 1) * cpb + c0);
         sq.x += t.x; sq.y += t.y; sq.z += t.z; sq.w += t.w;
       }
-      const float kq = sm[L.kqdot() + node];
+      const float kq = nsc.z;
       float4 o;
       o.x = fmaf(u.x, kq, g * sq.x);
       o.y = fmaf(u.y, kq, g * sq.y);
       o.z = fmaf(u.z, kq, g * sq.z);
       o.w = fmaf(u.w, kq, g * sq.w);
-      *reinterpret_cast<float4*>(p.out_o + (row * p.Hv + h) * p.dv + col) = o;
-      *reinterpret_cast<float4*>(p.u_out + (row * p.Hv + h) * p.dv + col) = u;
+      *reinterpret_cast<float4*>(o_base + node * node_stride) = o;
+      *reinterpret_cast<float4*>(u_base + node * node_stride) = u;
     }
 
     if constexpr (!kLeaf) {   // pass B (a leaf's new state is never used)
@@ -558,12 +557,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         materialise(g);        // the decay goes into the tile, as in advance()
         gam = 1.f;
       } else {
-        r = __frcp_rn(g);
+        r = __fdividef(1.f, g);
         gam = g;
       }
       update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
     }
-    if (tid == 0 && s == 0) p.a_out[row * p.Hv + h] = sm[L.a() + node];
   };
   using kT = std::true_type;
   using kF = std::false_type;
@@ -602,7 +600,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
       gam = 1.f;
     }
     preloaded = false;
-    const bool low = gam * sm[L.g() + node] < kGammaFloor;
+    const float4 nsc = *reinterpret_cast<const float4*>(sm + L.sc(node));
+    const float g = gam * nsc.x;   // gamma' of this node
+    const bool low = g < kGammaFloor;
     if (op & kOpLeaf) {
       // the boundary slot the next node reloads from, if it does so from HBM: loaded during this leaf
       int pre = -1;
@@ -614,11 +614,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
           pre = nsrc < p.nb_max ? nsrc : -1;
         }
       }
-      if (low) step(node, pre, kT{}, kT{});
-      else step(node, pre, kT{}, kF{});
+      if (low) step(node, pre, g, nsc, kT{}, kT{});
+      else step(node, pre, g, nsc, kT{}, kF{});
     } else {
-      if (low) step(node, -1, kF{}, kT{});
-      else step(node, -1, kF{}, kF{});
+      if (low) step(node, -1, g, nsc, kF{}, kT{});
+      else step(node, -1, g, nsc, kF{}, kF{});
     }
     if (op & kOpPush) {
       materialise(gam);
