@@ -2,9 +2,10 @@
 
 A step is one pass of the whole path over one batch: heavy-light schedules of
 every request's tree on the host and their upload, the verify call (pending
-commit folded into the conv window and the state tiles, every node advanced,
-boundary states and factors written) and the commit of each request's
-accepted path.  Default workload: 32 requests x 48 GDN layers of 48 v-heads
+commit folded into the conv window and the state tiles, every node solved in
+the tree-masked UT form, o and factors written; boundary states as scratch)
+and the commit of each request's accepted path.  The chain walk and the
+per-node-state baseline run afterwards on the same inputs as A/B legs.  Default workload: 32 requests x 48 GDN layers of 48 v-heads
 (d_k = d_v = 128, conv K = 4, bf16 inputs), a fresh 22-node top-4 DDTree per
 request and step, alternating factor banks.  The metric is verified tree nodes
 per second, one unit being one (request, GDN layer, v-head, node).
@@ -110,12 +111,12 @@ def algorithmic_bytes(w: S.Workload, n_per_req, nb_per_req, pend_len_per_req):
     return total
 
 
-def algorithmic_fma(w: S.Workload, n_per_req, leaves_per_req, pend_len_per_req):
+def algorithmic_fma(w: S.Workload, n_per_req, updates_per_req, pend_len_per_req):
     """FP32 multiply-adds of one verify call on the state tiles: per node T^T k and T^T q (2 per element),
-    the update (1 per element, not for leaves, whose new state is never read), 1 per element per folded
-    node.  The per-node vector work (u, o, normalisation, conv) is a few hundred operations per head and
-    is left out."""
-    per_elem = sum(2 * n + (n - lv) + L for n, lv, L in zip(n_per_req, leaves_per_req, pend_len_per_req))
+    1 per element for every node whose update is applied to a tile (none in the tree-masked UT form; the
+    non-leaf nodes when walking chains), 1 per element per folded node.  The per-node vector work (the
+    ancestor-pair solve, normalisation, conv) is a few thousand operations per head and is left out."""
+    per_elem = sum(2 * n + up + L for n, up, L in zip(n_per_req, updates_per_req, pend_len_per_req))
     return per_elem * w.layers * w.Hv * w.dk * w.dv
 
 
@@ -337,13 +338,12 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         s = i % w.steps
         n_req = [len(p) for p in plan.trees[s]]
         P, n = parents_host[s]
-        nb_req = hbm_stashes(N.gdn_pack_schedules(P, n)[0], w.n_max)   # boundary states are scratch
+        nb_req = [0] * w.B   # the tree-masked UT form writes no state but the committed one
         prev = plan.paths[(i - 1) % w.steps] if i > 0 else [[] for _ in range(w.B)]
         L_req = [len(p) for p in prev]
         units_per_step.append(sum(n_req) * w.layers * w.Hv)
         bytes_per_step.append(algorithmic_bytes(w, n_req, nb_req, L_req))
-        leaves = [int((np.bincount(p[1:], minlength=len(p)) == 0).sum()) if len(p) > 1 else 1 for p in plan.trees[s]]
-        fma_per_step.append(algorithmic_fma(w, n_req, leaves, L_req))
+        fma_per_step.append(algorithmic_fma(w, n_req, [0] * w.B, L_req))   # no per-node tile update in the UT form
 
     for i in range(args.warmup):
         one_step(i)
@@ -380,9 +380,10 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
 
     # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
     # A/B: the same steps with per-node-state schedules (every node reloads its parent's stored state)
-    ab = None
+    ab = walk = None
     if not args.no_ab:
-        ab = run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_step)
+        walk = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node=False)
+        ab = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node=True)
 
     if args.no_e2e:
         e2e = dict(ms=float("nan"), units=0, steps=0, h2d=0, d2h=0)
@@ -399,23 +400,25 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     avg_flops = 2 * statistics.mean(fma_per_step[args.warmup:])
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
                                 (clk or {}).get("sm_max_mhz") or 2070.0)
-    return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab,
+    return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab, walk=walk,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap,
                 gpu_launches=args.steps * 3)
 
 
-def run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_step):
-    """Per-node-state baseline on the same workload: schedules with no heavy edges, every node with
-    children stored and reloaded (the snapshot-style traffic the heavy-light chains avoid)."""
+def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node):
+    """The same workload verified by walking a schedule instead of the tree-masked UT form: the
+    heavy-light chains (branch states in tensor memory), or -- per_node -- the per-node-state baseline,
+    whose schedule has no heavy edges so every node with children is stored to and reloaded from HBM
+    (the snapshot-style traffic the heavy-light chains avoid)."""
     import torch
     from gated_deltanet_tree_gb300 import _native as N
     steps = max(2, min(args.steps, 10))
     packed, nb_cap = [], 1
     for s in range(w.steps):
         P, n = parents_host[s]
-        words, nb = N.gdn_pack_schedules_per_node(P, n)
+        words, nb = (N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules)(P, n)
         packed.append(torch.from_numpy(words).to(dev))
         nb_cap = max(nb_cap, nb)
     boundary = torch.empty(w.B, w.layers, nb_cap, w.Hv, w.dk, w.dv, dtype=torch.float32, device=dev)
@@ -426,7 +429,8 @@ def run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_ste
         sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=nb_cap, words=packed[s].data_ptr())
         X, BE, AG = gs.inputs[s]
         N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
-                          boundary, ver.banks, ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, stream)
+                          boundary, ver.banks, ver.workspace, ver.ws_bytes,
+                          N.GDN_VERIFY_BOUNDARY_SCRATCH | N.GDN_VERIFY_CHAIN_WALK, stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
 
     for i in range(3):
@@ -444,7 +448,8 @@ def run_per_node_ab(args, w, gs, dev, stream, paths, parents_host, units_per_ste
     ms = e0.elapsed_time(e1)
     del boundary
     torch.cuda.empty_cache()
-    return {"schedule": "per-node states (no heavy edges)", "steps": steps, "nb_max": nb_cap,
+    return {"schedule": "per-node states in HBM (no heavy edges)" if per_node else
+            "heavy-light chain walk, branch states in tensor memory", "steps": steps, "nb_max": nb_cap,
             "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
 
@@ -584,7 +589,7 @@ def main():
         "random activations; no model weights)", "config": config,
         "roofline": {"bound": "hbm" if r["avg_bytes"] / (r["peak"] * 1e9) >= r["avg_flops"] / (r["alu_peak"] * 1e12)
                      else "alu",
-                     "kernel": "gdn_tree_verify (conv_window_kernel + chain_verify_kernel)",
+                     "kernel": "gdn_tree_verify (conv_window_kernel + ut_verify_kernel)",
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
@@ -600,8 +605,11 @@ def main():
             "value": r["e2e_units"] / (r["e2e_ms"] / 1e3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
         "gpu_launches": r["gpu_launches"],
+        "ab_chain_walk": None if r["walk"] is None else dict(
+            r["walk"], ut_speedup=r["walk"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_per_node_states": None if r["ab"] is None else dict(
-            r["ab"], hld_speedup=r["ab"]["ms_per_step"] / (r["ms"] / args.steps)),
+            r["ab"], hld_speedup=r["ab"]["ms_per_step"] / r["walk"]["ms_per_step"],
+            ut_speedup=r["ab"]["ms_per_step"] / (r["ms"] / args.steps)),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -32,6 +32,7 @@ GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_COMMIT_COMPACT = 1
 GDN_VERIFY_BOUNDARY_SCRATCH = 1
+GDN_VERIFY_CHAIN_WALK = 2
 GDN_MAX_NODES = 64
 
 

@@ -149,7 +149,8 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
                            float* conv_state, float* out_o, float* boundary_states, gdn_banks* banks,
                            void* workspace, size_t workspace_bytes, int32_t flags, cudaStream_t stream) {
   gdn::clear_error();
-  if (flags & ~GDN_VERIFY_BOUNDARY_SCRATCH) return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
+  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK))
+    return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
   GDN_TRY(check_dims(d));
   GDN_TRY(check_sched(sched));
   if (layers < 1) return fail(GDN_ERR_INVALID_ARG, "layers = %d", layers);
@@ -197,13 +198,14 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   vp.u_out = banks->u[cur]; vp.a_out = banks->a[cur];
   vp.state = state; vp.out_o = out_o; vp.boundary = boundary_states;
   vp.boundary_out = (flags & GDN_VERIFY_BOUNDARY_SCRATCH) ? 0 : 1;
+  vp.chain_walk = (flags & GDN_VERIFY_CHAIN_WALK) ? 1 : 0;
   vp.fold = pend >= 0;
   if (pend >= 0) {
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];
   }
   vp.pend_path = banks->pend_path; vp.pend_len = banks->pend_len; vp.err = banks->err;
-  e = gdn::launch_verify(vp, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "chain-verify launch");
+  e = vp.chain_walk ? gdn::launch_verify(vp, stream) : gdn::launch_verify_ut(vp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, vp.chain_walk ? "chain-verify launch" : "tree-verify launch");
 
   banks->pend_bank = -1;
   banks->verified_bank = cur;

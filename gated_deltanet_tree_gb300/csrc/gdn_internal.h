@@ -123,6 +123,7 @@ struct VerifyParams {
   float* out_o;                // [B][L][n_max][Hv][dv]
   float* boundary;             // [B][L][nb_max][Hv][dk][dv]
   int boundary_out;            // store every boundary state (else the slots only take spills)
+  int chain_walk;              // the heavy-light chain walk (else the tree-masked UT form)
   int fold;
   const float* pend_k;
   const float* pend_u;
@@ -146,7 +147,8 @@ struct CommitParams {
 };
 
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);      // chain walk; also the fold-only launches
+cudaError_t launch_verify_ut(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form
 
 cudaError_t launch_commit(const CommitParams& p, int compact, cudaStream_t s);
 bool verify_supported(int dk, int dv);

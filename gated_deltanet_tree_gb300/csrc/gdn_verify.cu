@@ -49,42 +49,14 @@
 // materialisation wherever the accepted path enters a light child, where the
 // verify reloaded the stored state -- so the committed state reproduces, bit
 // for bit, the state the earlier verify stored for that node.
-#include <cuda_bf16.h>
-
 #include <type_traits>
 
-#include "gdn_internal.h"
+#include "gdn_tile.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kVerifyThreads = 128;
-constexpr int kCols = 4;           // columns per thread
-constexpr int kFoldChunk = 16;     // pending nodes staged per fold step
-constexpr float kGammaFloor = 1.0e-12f;   // below this the decay is applied to the tile at once
-
-typedef unsigned long long u64;
-
-__device__ __forceinline__ u64 pack2(float lo, float hi) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 unpack2(u64 v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-  u64 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
-  u64 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 // ---- tensor memory (tcgen05) as a stash for register tiles: the 32x32b access shape gives each
 // thread of a warp its own lane, so a tile held in registers moves in and out without crossing lanes.
@@ -103,41 +75,64 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
 }
 __device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// Loads 32 words of this thread's lane into 16 packed pairs; the wait is inside, so the
+// outputs are defined when the statement ends.
+__device__ __forceinline__ void tmem_get32(uint32_t ta, u64 (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "{\n"
+      " .reg .b32 t<32>;\n"
+      " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%16];\n"
+      " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%17];\n"
+      " tcgen05.wait::ld.sync.aligned;\n"
+      " mov.b64 %0, {t0, t1};\n"
+      " mov.b64 %1, {t2, t3};\n"
+      " mov.b64 %2, {t4, t5};\n"
+      " mov.b64 %3, {t6, t7};\n"
+      " mov.b64 %4, {t8, t9};\n"
+      " mov.b64 %5, {t10, t11};\n"
+      " mov.b64 %6, {t12, t13};\n"
+      " mov.b64 %7, {t14, t15};\n"
+      " mov.b64 %8, {t16, t17};\n"
+      " mov.b64 %9, {t18, t19};\n"
+      " mov.b64 %10, {t20, t21};\n"
+      " mov.b64 %11, {t22, t23};\n"
+      " mov.b64 %12, {t24, t25};\n"
+      " mov.b64 %13, {t26, t27};\n"
+      " mov.b64 %14, {t28, t29};\n"
+      " mov.b64 %15, {t30, t31};\n"
+      "}"
+      : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3]), "=l"(v[4]), "=l"(v[5]), "=l"(v[6]), "=l"(v[7]), "=l"(v[8]), "=l"(v[9]), "=l"(v[10]), "=l"(v[11]), "=l"(v[12]), "=l"(v[13]), "=l"(v[14]), "=l"(v[15])
+      : "r"(ta + 0u), "r"(ta + 16u)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// Stores 16 packed pairs as 32 words of this thread's lane and waits for the stores.
+__device__ __forceinline__ void tmem_put32(uint32_t ta, const u64 (&v)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
+      "{\n"
+      " .reg .b32 t<32>;\n"
+      " mov.b64 {t0, t1}, %0;\n"
+      " mov.b64 {t2, t3}, %1;\n"
+      " mov.b64 {t4, t5}, %2;\n"
+      " mov.b64 {t6, t7}, %3;\n"
+      " mov.b64 {t8, t9}, %4;\n"
+      " mov.b64 {t10, t11}, %5;\n"
+      " mov.b64 {t12, t13}, %6;\n"
+      " mov.b64 {t14, t15}, %7;\n"
+      " mov.b64 {t16, t17}, %8;\n"
+      " mov.b64 {t18, t19}, %9;\n"
+      " mov.b64 {t20, t21}, %10;\n"
+      " mov.b64 {t22, t23}, %11;\n"
+      " mov.b64 {t24, t25}, %12;\n"
+      " mov.b64 {t26, t27}, %13;\n"
+      " mov.b64 {t28, t29}, %14;\n"
+      " mov.b64 {t30, t31}, %15;\n"
+      " tcgen05.st.sync.aligned.32x32b.x16.b32 [%16], {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15};\n"
+      " tcgen05.st.sync.aligned.32x32b.x16.b32 [%17], {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31};\n"
+      " tcgen05.wait::st.sync.aligned;\n"
+      "}"
+      :
+      : "l"(v[0]), "l"(v[1]), "l"(v[2]), "l"(v[3]), "l"(v[4]), "l"(v[5]), "l"(v[6]), "l"(v[7]), "l"(v[8]), "l"(v[9]), "l"(v[10]), "l"(v[11]), "l"(v[12]), "l"(v[13]), "l"(v[14]), "l"(v[15]), "r"(ta + 0u), "r"(ta + 16u)
       : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// The loaded registers are defined only after tcgen05.wait::ld: tie them to a point after the wait so
-// that no use is scheduled before it.
-__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
-  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-               "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
-}
-
-template <typename InT>
-__device__ __forceinline__ float load_in(const InT* p, size_t i);
-template <>
-__device__ __forceinline__ float load_in<float>(const float* p, size_t i) {
-  return __ldg(p + i);
-}
-template <>
-__device__ __forceinline__ float load_in<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
-  return __bfloat162float(p[i]);
 }
 
 // Shared-memory layout (floats): tree region, fold region, then the schedule record (int32).
@@ -174,7 +169,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   constexpr int cpb = CPB;
   constexpr int kWords = 2 * kCols * NP;   // 32-bit words of a thread's tile = its tensor-memory columns per level
   static_assert(RPT % 4 == 0 && CG <= 32 && (DK / RPT) * CG % 32 == 0, "layout");
-  static_assert(kWords % 16 == 0 && (kCols * NP) % 8 == 0 && tmem_columns(kTmemLevels * kWords) <= 512, "stash");
+  static_assert(kWords % 32 == 0 && tmem_columns(kTmemLevels * kWords) <= 512, "stash");
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const Smem<DK> L{p.n_max, cpb};
@@ -200,89 +195,15 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
   const int row0 = rg * RPT;
   const size_t tile = static_cast<size_t>(DK) * p.dv;
 
-  // T[c][j] = (T[row0 + 2j][col + c], T[row0 + 2j + 1][col + c])
-  u64 T[kCols][NP];
-  auto load_tile = [&](const float* base) {
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const float4 r0 = *reinterpret_cast<const float4*>(base + static_cast<size_t>(2 * j) * p.dv);
-      const float4 r1 = *reinterpret_cast<const float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv);
-      T[0][j] = pack2(r0.x, r1.x);
-      T[1][j] = pack2(r0.y, r1.y);
-      T[2][j] = pack2(r0.z, r1.z);
-      T[3][j] = pack2(r0.w, r1.w);
-    }
-  };
-  auto store_tile = [&](float* base) {
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const float2 a0 = unpack2(T[0][j]), a1 = unpack2(T[1][j]), a2 = unpack2(T[2][j]), a3 = unpack2(T[3][j]);
-      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j) * p.dv) = make_float4(a0.x, a1.x, a2.x, a3.x);
-      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv) =
-          make_float4(a0.y, a1.y, a2.y, a3.y);
-    }
-  };
-  // pass B with the decay: T <- fmaf(k, u_c, g * T)
-  auto update = [&](const float* kvec, float g, float4 u) {
-    const u64 g2 = pack2(g, g);
-    const u64 u2[kCols] = {pack2(u.x, u.x), pack2(u.y, u.y), pack2(u.z, u.z), pack2(u.w, u.w)};
-    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
-#pragma unroll
-    for (int j4 = 0; j4 < NP / 2; ++j4) {
-      const ulonglong2 kk = k4[j4];
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        T[c][2 * j4 + 0] = fma2(kk.x, u2[c], mul2(g2, T[c][2 * j4 + 0]));
-        T[c][2 * j4 + 1] = fma2(kk.y, u2[c], mul2(g2, T[c][2 * j4 + 1]));
-      }
-    }
-  };
-  // pass B without the decay: T~ <- fmaf(k, ut_c, T~)
-  auto update_lazy = [&](const float* kvec, float4 ut) {
-    const u64 u2[kCols] = {pack2(ut.x, ut.x), pack2(ut.y, ut.y), pack2(ut.z, ut.z), pack2(ut.w, ut.w)};
-    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
-#pragma unroll
-    for (int j4 = 0; j4 < NP / 2; ++j4) {
-      const ulonglong2 kk = k4[j4];
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        T[c][2 * j4 + 0] = fma2(kk.x, u2[c], T[c][2 * j4 + 0]);
-        T[c][2 * j4 + 1] = fma2(kk.y, u2[c], T[c][2 * j4 + 1]);
-      }
-    }
-  };
-  // T~ <- gamma T~
-  auto materialise = [&](float gam) {
-    const u64 g2 = pack2(gam, gam);
-#pragma unroll
-    for (int c = 0; c < kCols; ++c)
-#pragma unroll
-      for (int j = 0; j < NP; ++j) T[c][j] = mul2(g2, T[c][j]);
-  };
-  // one node of the gated delta rule on the lazy tile; returns the new gamma.  Below the
-  // floor the decay goes into the tile first (the same mul-then-fma rounding as a direct
-  // decayed update), then the update is the plain one.
-  auto advance = [&](const float* kvec, float gam1, float4 u) -> float {
-    if (gam1 < kGammaFloor) {
-      materialise(gam1);
-      gam1 = 1.f;
-    }
-    const float r = __fdividef(1.f, gam1);
-    update_lazy(kvec, make_float4(u.x * r, u.y * r, u.z * r, u.w * r));
-    return gam1;
-  };
-  // store gamma T~ without touching the registers
-  auto store_scaled = [&](float* base, float gam) {
-    const u64 g2 = pack2(gam, gam);
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const float2 a0 = unpack2(mul2(g2, T[0][j])), a1 = unpack2(mul2(g2, T[1][j]));
-      const float2 a2 = unpack2(mul2(g2, T[2][j])), a3 = unpack2(mul2(g2, T[3][j]));
-      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j) * p.dv) = make_float4(a0.x, a1.x, a2.x, a3.x);
-      *reinterpret_cast<float4*>(base + static_cast<size_t>(2 * j + 1) * p.dv) =
-          make_float4(a0.y, a1.y, a2.y, a3.y);
-    }
-  };
+  // the thread's register tile (RegTile: RPT rows x 4 columns as packed row pairs)
+  RegTile<RPT> R;
+  auto& T = R.T;
+  auto load_tile = [&](const float* base) { R.load(base, p.dv); };
+  auto store_tile = [&](float* base) { R.store(base, p.dv); };
+  auto materialise = [&](float gam) { R.materialise(gam); };
+  auto update_lazy = [&](const float* kvec, float4 ut) { R.update_lazy(kvec + row0, ut); };
+  auto advance = [&](const float* kvec, float gam1, float4 u) -> float { return R.advance(kvec + row0, gam1, u); };
+  auto store_scaled = [&](float* base, float gam) { R.store_scaled(base, p.dv, gam); };
 
   float* st = p.state + (static_cast<size_t>(bl) * p.Hv + h) * tile + static_cast<size_t>(row0) * p.dv + col;
 
@@ -422,38 +343,28 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
                     static_cast<size_t>(row0) * p.dv + col;
   int parity = 0;
   const size_t slot_stride = static_cast<size_t>(p.Hv) * tile;
-  const u64 zero2 = pack2(0.f, 0.f);
 
   // ---- stash moves between the register tile and tensor memory
   auto tmem_put = [&](int level) {
     const uint32_t ta = tthread + static_cast<uint32_t>(level * kWords);
     __syncwarp();   // the warp-collective tcgen05 accesses run converged
 #pragma unroll
-    for (int q = 0; q < kWords / 16; ++q) {
-      uint32_t r[16];
+    for (int half = 0; half < kWords / 32; ++half) {   // 32 words per statement
+      u64 v[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 f = unpack2(T[(q * 8 + e) / NP][(q * 8 + e) % NP]);
-        r[2 * e] = __float_as_uint(f.x);
-        r[2 * e + 1] = __float_as_uint(f.y);
-      }
-      tmem_st16(ta + 16 * q, r);
+      for (int f = 0; f < 16; ++f) v[f] = T[(16 * half + f) / NP][(16 * half + f) % NP];
+      tmem_put32(ta + 32u * half, v);
     }
-    tmem_wait_st();
   };
   auto tmem_get = [&](int level) {
     const uint32_t ta = tthread + static_cast<uint32_t>(level * kWords);
     __syncwarp();
-    uint32_t r[kWords / 16][16];
 #pragma unroll
-    for (int q = 0; q < kWords / 16; ++q) tmem_ld16(ta + 16 * q, r[q]);
-    tmem_wait_ld();
+    for (int half = 0; half < kWords / 32; ++half) {
+      u64 v[16];
+      tmem_get32(ta + 32u * half, v);
 #pragma unroll
-    for (int q = 0; q < kWords / 16; ++q) {
-      reg_fence16(r[q]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        T[(q * 8 + e) / NP][(q * 8 + e) % NP] = pack2(__uint_as_float(r[q][2 * e]), __uint_as_float(r[q][2 * e + 1]));
+      for (int f = 0; f < 16; ++f) T[(16 * half + f) / NP][(16 * half + f) % NP] = v[f];
     }
   };
 
@@ -467,25 +378,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
     constexpr bool kLeaf = decltype(leaf_t)::value;
     constexpr bool kLow = decltype(low_t)::value;
     const float* kvec = sm + L.kq(node);
-    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kvec + row0);
-    const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(kvec + DK + row0);
 
     // pass A on the state before this node
     u64 ak[kCols], aq[kCols];
-#pragma unroll
-    for (int cc = 0; cc < kCols; ++cc) ak[cc] = aq[cc] = zero2;
-#pragma unroll
-    for (int j4 = 0; j4 < NP / 2; ++j4) {
-      const ulonglong2 kk = k4[j4];
-      const ulonglong2 qq = q4[j4];
-#pragma unroll
-      for (int cc = 0; cc < kCols; ++cc) {
-        ak[cc] = fma2(T[cc][2 * j4 + 0], kk.x, ak[cc]);
-        aq[cc] = fma2(T[cc][2 * j4 + 0], qq.x, aq[cc]);
-        ak[cc] = fma2(T[cc][2 * j4 + 1], kk.y, ak[cc]);
-        aq[cc] = fma2(T[cc][2 * j4 + 1], qq.y, aq[cc]);
-      }
-    }
+    R.dots(kvec + row0, kvec + DK + row0, ak, aq);
     // A leaf's updated state is never read (the fold rebuilds it from the factor bank), so the tile
     // is free after pass A: when the next node reloads a stash from HBM, start that load now, under
     // this node's reduction.
@@ -495,13 +391,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) chain_verify_kernel(VerifyP
         preloaded = true;
       }
     }
-    float4 sk, sq;
-    {
-      const float2 a0 = unpack2(ak[0]), a1 = unpack2(ak[1]), a2 = unpack2(ak[2]), a3 = unpack2(ak[3]);
-      const float2 b0 = unpack2(aq[0]), b1 = unpack2(aq[1]), b2 = unpack2(aq[2]), b3 = unpack2(aq[3]);
-      sk = make_float4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y);
-      sq = make_float4(b0.x + b0.y, b1.x + b1.y, b2.x + b2.y, b3.x + b3.y);
-    }
+    float4 sk = fold_pairs(ak), sq = fold_pairs(aq);
     // row groups of this warp
 #pragma unroll
     for (int m = CG; m < 32; m <<= 1) {

@@ -31,9 +31,11 @@ class WorkloadPlan:
     """Trees and accepted paths of every step (host), generated up front."""
 
     def __init__(self, w: S.Workload, trees: Optional[List[List[np.ndarray]]] = None,
-                 paths: Optional[List[List[np.ndarray]]] = None, per_node: bool = False):
+                 paths: Optional[List[List[np.ndarray]]] = None, per_node: bool = False,
+                 chain_walk: bool = False):
         self.w = w
         self.per_node = per_node   # per-node-state schedules instead of heavy-light ones
+        self.chain_walk = chain_walk or per_node   # walk the schedule's chains (else the tree-masked UT form)
         self.trees = trees if trees is not None else [S.step_trees(w, s) for s in range(w.steps)]
         self.paths = paths if paths is not None else [S.step_paths(w, self.trees[s], s) for s in range(w.steps)]
         self.nb_cap = 0
@@ -111,7 +113,7 @@ class GpuSession:
     def verify(self, step: int, stream=None, boundary_scratch: bool = False):
         X, BE, AG = self.step_inputs(step)
         self.ver.verify(self.schedule(step), X, self.conv_w, BE, AG, self.state, self.conv_state, self.out_o,
-                        self.boundary, stream, boundary_scratch)
+                        self.boundary, stream, boundary_scratch, self.plan.chain_walk)
 
     def local_layer(self, l: int) -> int:
         return self.layer_ids.index(l)

@@ -236,6 +236,7 @@ gdn_status gdn_banks_init(gdn_banks* banks, int32_t B, int32_t layers, int32_t n
 size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t n_max);
 
 #define GDN_VERIFY_BOUNDARY_SCRATCH 1   /* boundary_states is scratch, not output */
+#define GDN_VERIFY_CHAIN_WALK 2         /* walk the heavy-light chains instead of the tree-masked UT form */
 
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify -- fold the pending path, then verify a batch of trees.
@@ -261,7 +262,13 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              With GDN_VERIFY_BOUNDARY_SCRATCH in flags it is scratch instead: only
  *              stashes that spill out of tensor memory are written there, and its
  *              contents are unspecified on return.
- *   flags      0 or GDN_VERIFY_BOUNDARY_SCRATCH (other bits: GDN_ERR_INVALID_ARG)
+ *   flags      GDN_VERIFY_BOUNDARY_SCRATCH and/or GDN_VERIFY_CHAIN_WALK (other bits:
+ *              GDN_ERR_INVALID_ARG).  By default the nodes are solved in the tree-masked
+ *              UT form (article "状态驻留验证": the topology-masked UT decomposition): one
+ *              sweep of the committed state per node, no dependency between nodes, then a
+ *              forward substitution over ancestor pairs.  GDN_VERIFY_CHAIN_WALK walks the
+ *              packed ops instead: heavy-light chains in registers, branch states stashed in
+ *              tensor memory.  Both give the same results up to rounding.
  *   banks      factors of every node are written into bank write_bank
  *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
  * Rows of nodes >= n[b] are neither read nor written.

@@ -67,10 +67,10 @@ def test_algorithmic_bytes_by_hand():
 
 
 def test_algorithmic_fma_by_hand():
-    # 2 requests, 1 layer, Hv=2, d=4: n=3 with 2 leaves and L=1; n=1 (a leaf) and L=0
+    # 2 requests, 1 layer, Hv=2, d=4: n=3 with 1 tile update and L=1; n=1 with none and L=0
     w = S.workload(1).replace(B=2, layers=1, Hk=1, Hv=2, dk=4, dv=4)
-    per_elem = (2 * 3 + (3 - 2) + 1) + (2 * 1 + 0 + 0)
-    assert bench.algorithmic_fma(w, [3, 1], [2, 1], [1, 0]) == per_elem * 2 * 4 * 4
+    per_elem = (2 * 3 + 1 + 1) + (2 * 1 + 0 + 0)
+    assert bench.algorithmic_fma(w, [3, 1], [1, 0], [1, 0]) == per_elem * 2 * 4 * 4
     assert abs(bench.fp32_peak_tflops(152, 2070.0) - 80.55) < 0.01
 
 
