@@ -309,13 +309,16 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         parents_host.append((P, n))
     paths = [gs.paths(s) for s in range(w.steps)]
 
+    depth_of = [0] * w.steps   # the deepest node of each step's trees (it selects the verify kernel)
+
     def sched_struct(s):
-        return N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, words=words_dev[s].data_ptr())
+        return N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, depth_max=depth_of[s],
+                                    words=words_dev[s].data_ptr())
 
     def one_step(i, timing=None):
         s = i % w.steps
         P, n = parents_host[s]
-        words, _ = N.gdn_pack_schedules(P, n)                       # host heavy-light schedules
+        words, _, depth_of[s] = N.gdn_pack_schedules(P, n, with_depth=True)   # host heavy-light schedules
         words_host[s].numpy()[...] = words
         words_dev[s].copy_(words_host[s], non_blocking=True)
         X, BE, AG = gs.inputs[s]
@@ -487,7 +490,7 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
     for k in range(steps):
         i, s = k % 2, k % nsrc
         P, n = parents_host[s]
-        words, _ = N.gdn_pack_schedules(P, n)            # host heavy-light schedules
+        words, _, depth = N.gdn_pack_schedules(P, n, with_depth=True)   # host heavy-light schedules
         wh[k].numpy()[...] = words
         with torch.cuda.stream(s_h2d):
             if k >= 2:
@@ -499,7 +502,7 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
         stream.wait_event(h2d_done[k])
         if k >= 2:
             stream.wait_event(d2h_done[k - 2])           # output buffer i downloaded
-        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, words=wd[i].data_ptr())
+        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=gs.nb_cap, depth_max=depth, words=wd[i].data_ptr())
         X_d, BE_d, AG_d = dev_in[i]
         N.gdn_tree_verify(gs.dims, w.layers, sc, X_d, gs.conv_w, BE_d, AG_d, gs.state, gs.conv_state, out[i],
                           gs.boundary, ver.banks, ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, stream)

@@ -58,7 +58,7 @@ class gdn_schedule(ctypes.Structure):
 
 
 class gdn_batch_schedule(ctypes.Structure):
-    _fields_ = [("B", c_i32), ("n_max", c_i32), ("nb_max", c_i32), ("words", c_p)]
+    _fields_ = [("B", c_i32), ("n_max", c_i32), ("nb_max", c_i32), ("depth_max", c_i32), ("words", c_p)]
 
 
 class gdn_banks(ctypes.Structure):
@@ -83,8 +83,8 @@ def lib():
         L.gdn_hld_schedule.argtypes = [P(c_i32), c_i32, P(gdn_schedule)]
         L.gdn_schedule_words.argtypes = [c_i32]
         L.gdn_schedule_words.restype = c_i32
-        L.gdn_pack_schedules.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
-        L.gdn_pack_schedules_per_node.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32)]
+        L.gdn_pack_schedules.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32), P(c_i32)]
+        L.gdn_pack_schedules_per_node.argtypes = [P(c_i32), P(c_i32), c_i32, c_i32, P(c_i32), P(c_i32), P(c_i32)]
         L.gdn_ddtree_build.argtypes = [P(ctypes.c_float), c_i32, c_i32, c_i32, ctypes.c_double, c_i32, P(c_i32),
                                        P(c_i32), P(c_i32), P(ctypes.c_double), P(c_i32)]
         L.gdn_ddtree_build_batch.argtypes = [P(ctypes.c_float), c_i32, c_i32, c_i32, c_i32, ctypes.c_double, c_i32,
@@ -159,30 +159,27 @@ def gdn_schedule_words(n_max: int) -> int:
     return lib().gdn_schedule_words(n_max)
 
 
-def gdn_pack_schedules(parents: np.ndarray, n: np.ndarray):
-    """parents [B, n_max] int32 (rows padded with anything past n[b]), n [B] -> (words [B, W] int32, nb_max)."""
+def _pack(fn, parents: np.ndarray, n: np.ndarray, with_depth: bool):
     parents = np.ascontiguousarray(parents, dtype=np.int32)
     n = np.ascontiguousarray(n, dtype=np.int32)
     B, n_max = parents.shape
     words = np.empty((B, gdn_schedule_words(n_max)), dtype=np.int32)
-    nb = c_i32(0)
+    nb, depth = c_i32(0), c_i32(0)
     P = ctypes.POINTER(c_i32)
-    _check(lib().gdn_pack_schedules(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max,
-                                    words.ctypes.data_as(P), ctypes.byref(nb)))
-    return words, int(nb.value)
+    _check(fn(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max, words.ctypes.data_as(P), ctypes.byref(nb),
+              ctypes.byref(depth)))
+    return (words, int(nb.value), int(depth.value)) if with_depth else (words, int(nb.value))
 
 
-def gdn_pack_schedules_per_node(parents: np.ndarray, n: np.ndarray):
-    """Per-node-state schedule (every node its own chain) in the packed layout -> (words, nb_max)."""
-    parents = np.ascontiguousarray(parents, dtype=np.int32)
-    n = np.ascontiguousarray(n, dtype=np.int32)
-    B, n_max = parents.shape
-    words = np.empty((B, gdn_schedule_words(n_max)), dtype=np.int32)
-    nb = c_i32(0)
-    P = ctypes.POINTER(c_i32)
-    _check(lib().gdn_pack_schedules_per_node(parents.ctypes.data_as(P), n.ctypes.data_as(P), B, n_max,
-                                             words.ctypes.data_as(P), ctypes.byref(nb)))
-    return words, int(nb.value)
+def gdn_pack_schedules(parents: np.ndarray, n: np.ndarray, with_depth: bool = False):
+    """parents [B, n_max] int32 (rows padded with anything past n[b]), n [B] -> (words [B, W] int32, nb_max),
+    and the deepest node's depth as a third value with with_depth."""
+    return _pack(lib().gdn_pack_schedules, parents, n, with_depth)
+
+
+def gdn_pack_schedules_per_node(parents: np.ndarray, n: np.ndarray, with_depth: bool = False):
+    """Per-node-state schedule in the packed layout -> (words, nb_max[, depth_max])."""
+    return _pack(lib().gdn_pack_schedules_per_node, parents, n, with_depth)
 
 
 GDN_DDTREE_CHAIN_SEED = 1

@@ -198,7 +198,8 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   vp.u_out = banks->u[cur]; vp.a_out = banks->a[cur];
   vp.state = state; vp.out_o = out_o; vp.boundary = boundary_states;
   vp.boundary_out = (flags & GDN_VERIFY_BOUNDARY_SCRATCH) ? 0 : 1;
-  vp.chain_walk = (flags & GDN_VERIFY_CHAIN_WALK) ? 1 : 0;
+  // the UT form costs depth^2 per node and depth per (node, column): deep trees walk their chains
+  vp.chain_walk = ((flags & GDN_VERIFY_CHAIN_WALK) || sched->depth_max > GDN_UT_MAX_DEPTH) ? 1 : 0;
   vp.fold = pend >= 0;
   if (pend >= 0) {
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];

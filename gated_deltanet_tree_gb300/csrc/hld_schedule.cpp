@@ -243,15 +243,27 @@ static gdn_status pack_per_node(const int32_t* parent, int n, const gdn::SchedLa
   return GDN_OK;
 }
 
+// Depth of the deepest node of a valid tree (parent[i] < i).
+static int tree_depth(const int32_t* parent, int n) {
+  std::vector<int> depth(n, 0);
+  int m = 0;
+  for (int i = 1; i < n; ++i) {
+    depth[i] = depth[parent[i]] + 1;
+    m = depth[i] > m ? depth[i] : m;
+  }
+  return m;
+}
+
 extern "C" gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const int32_t* n, int32_t B,
-                                                  int32_t n_max, int32_t* words, int32_t* nb_max_out) {
+                                                  int32_t n_max, int32_t* words, int32_t* nb_max_out,
+                                                  int32_t* depth_max_out) {
   gdn::clear_error();
   if (!parents || !n || !words) return fail(GDN_ERR_INVALID_ARG, "NULL argument to gdn_pack_schedules_per_node");
   if (B < 1) return fail(GDN_ERR_INVALID_ARG, "B = %d", B);
   if (n_max < 1 || n_max > GDN_MAX_NODES)
     return fail(GDN_ERR_UNSUPPORTED, "n_max = %d outside 1..%d", n_max, GDN_MAX_NODES);
   const gdn::SchedLayout lay{n_max};
-  int nb_max = 0;
+  int nb_max = 0, depth_max = 0;
   for (int b = 0; b < B; ++b) {
     if (n[b] < 1 || n[b] > n_max)
       return fail(GDN_ERR_INVALID_TREE, "request %d: n = %d outside 1..n_max (%d)", b, n[b], n_max);
@@ -260,20 +272,23 @@ extern "C" gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const 
                                   words + static_cast<size_t>(b) * lay.words(), &nb);
     if (st != GDN_OK) return st;
     nb_max = nb > nb_max ? nb : nb_max;
+    const int dp = tree_depth(parents + static_cast<size_t>(b) * n_max, n[b]);
+    depth_max = dp > depth_max ? dp : depth_max;
   }
   if (nb_max_out) *nb_max_out = nb_max;
+  if (depth_max_out) *depth_max_out = depth_max;
   return GDN_OK;
 }
 
 extern "C" gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
-                                         int32_t* words, int32_t* nb_max_out) {
+                                         int32_t* words, int32_t* nb_max_out, int32_t* depth_max_out) {
   gdn::clear_error();
   if (!parents || !n || !words) return fail(GDN_ERR_INVALID_ARG, "NULL argument to gdn_pack_schedules");
   if (B < 1) return fail(GDN_ERR_INVALID_ARG, "B = %d", B);
   if (n_max < 1 || n_max > GDN_MAX_NODES)
     return fail(GDN_ERR_UNSUPPORTED, "n_max = %d outside 1..%d", n_max, GDN_MAX_NODES);
   const gdn::SchedLayout lay{n_max};
-  int nb_max = 0;
+  int nb_max = 0, depth_max = 0;
   Hld h;
   for (int b = 0; b < B; ++b) {
     if (n[b] < 1 || n[b] > n_max)
@@ -283,7 +298,10 @@ extern "C" gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* 
     write_record(parents + static_cast<size_t>(b) * n_max, h.n, lay, h.n_chains, h.n_boundary, h.n_waves, h.bslot,
                  h.heavy.data(), false, words + static_cast<size_t>(b) * lay.words());
     if (h.n_boundary > nb_max) nb_max = h.n_boundary;
+    const int dp = tree_depth(parents + static_cast<size_t>(b) * n_max, h.n);
+    depth_max = dp > depth_max ? dp : depth_max;
   }
   if (nb_max_out) *nb_max_out = nb_max;
+  if (depth_max_out) *depth_max_out = depth_max;
   return GDN_OK;
 }

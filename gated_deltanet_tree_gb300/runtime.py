@@ -35,15 +35,17 @@ class DeviceSchedule:
             P[b, :len(p)] = p
             n[b] = len(p)
         pack = N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules
-        words, nb = pack(P, n)
+        words, nb, depth = pack(P, n, with_depth=True)
         self.parents, self.n, self.nb_max = P, n, nb if nb_cap is None else max(nb, nb_cap)
+        self.depth_max = depth
         if words_out is None:
             self.words = torch.from_numpy(words).to(device)
         else:
             words_out.copy_(torch.from_numpy(words), non_blocking=False)
             self.words = words_out
         self.host_words = words
-        self.struct = N.gdn_batch_schedule(B=B, n_max=n_max, nb_max=self.nb_max, words=self.words.data_ptr())
+        self.struct = N.gdn_batch_schedule(B=B, n_max=n_max, nb_max=self.nb_max, depth_max=depth,
+                                           words=self.words.data_ptr())
 
 
 class TreeVerifier:

@@ -36,6 +36,7 @@ class WorkloadPlan:
         self.w = w
         self.per_node = per_node   # per-node-state schedules instead of heavy-light ones
         self.chain_walk = chain_walk or per_node   # walk the schedule's chains (else the tree-masked UT form)
+        self.depth_hint = True   # pass the trees' depth, which sends trees deeper than GDN_UT_MAX_DEPTH to the walk
         self.trees = trees if trees is not None else [S.step_trees(w, s) for s in range(w.steps)]
         self.paths = paths if paths is not None else [S.step_paths(w, self.trees[s], s) for s in range(w.steps)]
         self.nb_cap = 0
@@ -103,6 +104,8 @@ class GpuSession:
         if step not in self.scheds:
             self.scheds[step] = self.ver.schedule(self.plan.trees[step], nb_cap=self.nb_cap,
                                                   per_node=self.plan.per_node)
+            if not self.plan.depth_hint:
+                self.scheds[step].struct.depth_max = 0
         return self.scheds[step]
 
     def paths(self, step: int):

@@ -138,13 +138,14 @@ gdn_status gdn_hld_schedule(const int32_t* parent, int32_t n, gdn_schedule* out)
  * ones spill to the node's boundary slot.
  * gdn_pack_schedules runs gdn_hld_schedule on every request's tree and writes
  * the records into words_host (B * gdn_schedule_words(n_max) int32, caller-
- * owned host memory); *nb_max_out receives the largest boundary count.  The
+ * owned host memory); *nb_max_out receives the largest boundary count and
+ * *depth_max_out the depth of the deepest node (either may be NULL).  The
  * caller copies the words to the device and fills a gdn_batch_schedule.
  * parents: B rows of n_max entries; n[b] nodes of request b are used.
  * ------------------------------------------------------------------------- */
 int32_t gdn_schedule_words(int32_t n_max);
 gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
-                              int32_t* words_host, int32_t* nb_max_out);
+                              int32_t* words_host, int32_t* nb_max_out, int32_t* depth_max_out);
 
 /* Per-node-state schedule in the same packed layout, for comparison with the heavy-light one: every node
  * with children stashes its state in its boundary slot (in HBM) and every child reloads it from there -- the
@@ -152,7 +153,7 @@ gdn_status gdn_pack_schedules(const int32_t* parents, const int32_t* n, int32_t 
  * instead of twice per chain).  The walk is depth first, children by index.  Same arguments and results as
  * gdn_pack_schedules; nb_max is the number of nodes with children. */
 gdn_status gdn_pack_schedules_per_node(const int32_t* parents, const int32_t* n, int32_t B, int32_t n_max,
-                                       int32_t* words_host, int32_t* nb_max_out);
+                                       int32_t* words_host, int32_t* nb_max_out, int32_t* depth_max_out);
 
 /* ---------------------------------------------------------------------------
  * DDTree construction with confidence pruning (host, pure).
@@ -193,8 +194,11 @@ typedef struct {
   int32_t B;               /* requests */
   int32_t n_max;           /* node stride of every per-node array */
   int32_t nb_max;          /* slot stride of boundary_states (>= every request's n_boundary) */
+  int32_t depth_max;       /* deepest node of any tree, as the packers return it (0: unknown); trees
+                              deeper than GDN_UT_MAX_DEPTH verify by walking chains (gdn_tree_verify) */
   const int32_t* words;    /* device, B * gdn_schedule_words(n_max) int32 */
 } gdn_batch_schedule;
+#define GDN_UT_MAX_DEPTH 24
 
 /* ---------------------------------------------------------------------------
  * Double-buffered FP32 factor banks (SpecLA article, "接受因子缓存": per node
@@ -268,7 +272,9 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              sweep of the committed state per node, no dependency between nodes, then a
  *              forward substitution over ancestor pairs.  GDN_VERIFY_CHAIN_WALK walks the
  *              packed ops instead: heavy-light chains in registers, branch states stashed in
- *              tensor memory.  Both give the same results up to rounding.
+ *              tensor memory.  Both give the same results up to rounding.  Batches whose
+ *              sched->depth_max exceeds GDN_UT_MAX_DEPTH walk chains without the flag: the
+ *              UT form's per-node work grows with the square of the depth.
  *   banks      factors of every node are written into bank write_bank
  *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
  * Rows of nodes >= n[b] are neither read nor written.

@@ -205,8 +205,12 @@ def test_qwen_like_single_layer(chain_walk):
 @pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
 def test_chain64_single_layer(chain_walk):
     # the pure-chain shape of the stress workload: 64-node chain, chain acceptance of the whole walk
+    # the UT form would hand a 63-deep chain to the walk; here it is made to solve it itself
+    from harness import WorkloadPlan
     w = S.workload(6).replace(B=2, layers=1, steps=2)
-    run_parity(w, chain_walk=chain_walk)
+    plan = WorkloadPlan(w)
+    plan.depth_hint = chain_walk
+    run_parity(w, plan=plan, chain_walk=chain_walk)
 
 
 @pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
