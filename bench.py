@@ -38,6 +38,7 @@ import synthetic as S  # noqa: E402
 
 METRIC = "verified tree-nodes/sec (GDN layer·head·node) and achieved HBM GB/s vs GB300 peak"
 UNIT = "nodes/s"
+UT_MAX_DEPTH = 24   # GDN_UT_MAX_DEPTH: deeper batches are verified by walking chains
 
 
 def measured_traffic():
@@ -109,6 +110,13 @@ def algorithmic_bytes(w: S.Workload, n_per_req, nb_per_req, pend_len_per_req):
     if w.conv_mode:
         total += w.layers * C * w.K * 4               # conv weights
     return total
+
+
+def tree_depth(parent) -> int:
+    depth = [0] * len(parent)
+    for i in range(1, len(parent)):
+        depth[i] = depth[parent[i]] + 1
+    return max(depth)
 
 
 def algorithmic_fma(w: S.Workload, n_per_req, updates_per_req, pend_len_per_req):
@@ -336,7 +344,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
             dist.barrier()
 
     # bytes / units of each step (pending length of step s = accepted path length of step s-1)
-    units_per_step, bytes_per_step, fma_per_step = [], [], []
+    units_per_step, bytes_per_step, fma_per_step, walks = [], [], [], []
     for i in range(args.warmup + args.steps):
         s = i % w.steps
         n_req = [len(p) for p in plan.trees[s]]
@@ -346,7 +354,13 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         L_req = [len(p) for p in prev]
         units_per_step.append(sum(n_req) * w.layers * w.Hv)
         bytes_per_step.append(algorithmic_bytes(w, n_req, nb_req, L_req))
-        fma_per_step.append(algorithmic_fma(w, n_req, [0] * w.B, L_req))   # no per-node tile update in the UT form
+        walk = max(tree_depth(p) for p in plan.trees[s]) > UT_MAX_DEPTH   # deep trees walk chains
+        walks.append(walk)
+        if walk:   # the chain walk updates the tile at every node with children
+            ups = [int((np.bincount(p[1:], minlength=len(p)) > 0).sum()) if len(p) > 1 else 0 for p in plan.trees[s]]
+        else:      # the tree-masked UT form applies no per-node update to the tile
+            ups = [0] * w.B
+        fma_per_step.append(algorithmic_fma(w, n_req, ups, L_req))
 
     for i in range(args.warmup):
         one_step(i)
@@ -406,7 +420,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab, walk=walk,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
-                e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap,
+                e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap, walked=any(walks[args.warmup:]),
                 gpu_launches=args.steps * 3)
 
 
@@ -592,7 +606,8 @@ def main():
         "random activations; no model weights)", "config": config,
         "roofline": {"bound": "hbm" if r["avg_bytes"] / (r["peak"] * 1e9) >= r["avg_flops"] / (r["alu_peak"] * 1e12)
                      else "alu",
-                     "kernel": "gdn_tree_verify (conv_window_kernel + ut_verify_kernel)",
+                     "kernel": "gdn_tree_verify (conv_window_kernel + "
+                               + ("chain_verify_kernel)" if r["walked"] else "ut_verify_kernel)"),
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
