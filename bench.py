@@ -406,7 +406,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
         e2e = dict(ms=float("nan"), units=0, steps=0, h2d=0, d2h=0)
     else:
         e2e = run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct,
-                      units_per_step)
+                      units_per_step, rank)
 
     ms, timed_units_all, e2e_ms, e2e_units_all = reduce_across_ranks(ms, timed_units, e2e["ms"], e2e["units"], dev)
 
@@ -470,14 +470,20 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node):
             "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
 
-def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct, units_per_step):
-    """Same calls with host buffers: each step copies its inputs from pinned host memory and reads its
-    outputs back.  Copies run on their own streams, double-buffered, so step k+1's upload and step k-1's
-    download overlap step k's compute; the timed span runs from the first upload to the last download."""
+def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev, sched_struct, units_per_step,
+            rank=0):
+    """Same calls with host buffers: each step builds its trees from the draft's log-probabilities (the
+    DDTree builder, for DDTree workloads), packs their schedules, copies its inputs from pinned host memory
+    and reads its outputs back.  Copies run on their own streams, double-buffered, so step k+1's upload
+    and step k-1's download overlap step k's compute; the timed span runs from the first upload to the
+    last download."""
     import torch
     from gated_deltanet_tree_gb300 import _native as N
     steps = max(1, min(args.steps, 8))
     nsrc = min(2, w.steps)
+    drafts = None
+    if w.tree == "ddtree":   # draft tables of the requests served (the trees are rebuilt from them each step)
+        drafts = [np.stack([S.draft_logp(w, b + rank * w.B, s) for b in range(w.B)]) for s in range(nsrc)]
     host_in = []
     for s in range(nsrc):
         X, BE, AG = gs.inputs[s]
@@ -503,7 +509,10 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
     e0.record(s_h2d)
     for k in range(steps):
         i, s = k % 2, k % nsrc
-        P, n = parents_host[s]
+        if drafts is not None:
+            P, n = N.gdn_ddtree_build_batch(drafts[s], w.budget, w.n_max)   # host DDTree construction
+        else:
+            P, n = parents_host[s]
         words, _, depth = N.gdn_pack_schedules(P, n, with_depth=True)   # host heavy-light schedules
         wh[k].numpy()[...] = words
         with torch.cuda.stream(s_h2d):
@@ -526,7 +535,7 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
             s_d2h.wait_event(cmp_done[k])
             o_host[i].copy_(out[i], non_blocking=True)
             d2h_done[k].record(s_d2h)
-        units += units_per_step[s]
+        units += int(np.asarray(n).sum()) * w.layers * w.Hv
     s_d2h.wait_event(d2h_done[steps - 1])
     e1.record(s_d2h)
     torch.cuda.synchronize(dev)
@@ -621,7 +630,9 @@ def main():
         "clocks": r["clocks"],
         "e2e": None if args.no_e2e else {
             "value": r["e2e_units"] / (r["e2e_ms"] / 1e3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
-            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
+            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
+            "host_per_step": ("DDTree construction from the draft tables, " if w.tree == "ddtree" else "")
+                             + "heavy-light schedules, packing"},
         "gpu_launches": r["gpu_launches"],
         "ab_chain_walk": None if r["walk"] is None else dict(
             r["walk"], ut_speedup=r["walk"]["ms_per_step"] / (r["ms"] / args.steps)),

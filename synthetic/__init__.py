@@ -279,6 +279,16 @@ def tree_for(w: Workload, b: int, step: int) -> np.ndarray:
     raise ValueError(w.tree)
 
 
+def draft_logp(w: Workload, b: int, step: int) -> np.ndarray:
+    """The synthetic draft's per-depth top-K log-probabilities behind tree_for's DDTree, [depth_max][top_k]
+    fp32 (row d-1 = depth d), drawn from the same stream as the tree."""
+    rng = rng_for(w.cfg, S_TREE, b, step)
+    z = np.sort(rng.normal(0.0, 2.0, size=(w.depth_max + 1, w.top_k)), axis=1)[:, ::-1]
+    m = z.max(axis=1, keepdims=True)
+    logp = z - (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))
+    return np.ascontiguousarray(logp[1:], dtype=np.float32)
+
+
 def path_for(w: Workload, parent: np.ndarray, b: int, step: int) -> np.ndarray:
     rng = rng_for(w.cfg, S_PATH, b, step)
     if w.path == 'walk':

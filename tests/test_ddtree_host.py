@@ -90,3 +90,16 @@ def test_rejects_bad_arguments(N):
     with pytest.raises(N.GdnError) as e:
         N.gdn_ddtree_build_batch(ok[None], 8, 4)
     assert e.value.status == N.GDN_ERR_INVALID_ARG
+
+
+def test_rebuilds_the_workload_trees_from_their_draft_tables(N):
+    # the batched workload's trees come from a separate Python generator; built from the same draws by the
+    # library they come out identical (DFS numbering included)
+    import synthetic as S
+    for cfg in (4, 5):
+        w = S.workload(cfg)
+        for step in range(2):
+            lp = np.stack([S.draft_logp(w, b, step) for b in range(8)])
+            parents, n = N.gdn_ddtree_build_batch(lp, w.budget, w.n_max)
+            for b in range(8):
+                assert parents[b, :n[b]].tolist() == S.tree_for(w, b, step).tolist()
