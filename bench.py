@@ -66,6 +66,16 @@ def measured_traffic():
         return None
 
 
+def tf32_peak() -> float:
+    """Dense tf32 tensor peak (TFLOP/s): the measured bf16 burst GEMM rate times the nominal tf32 : bf16
+    ratio (1.1 : 2.25 PFLOP/s dense, taken as 1/2); the nominal 1.1 PFLOP/s if nothing was measured."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]) / 2
+    except Exception:
+        return 1100.0
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -126,6 +136,25 @@ def algorithmic_fma(w: S.Workload, n_per_req, updates_per_req, pend_len_per_req)
     ancestor-pair solve, normalisation, conv) is a few thousand operations per head and is left out."""
     per_elem = sum(2 * n + up + L for n, up, L in zip(n_per_req, updates_per_req, pend_len_per_req))
     return per_elem * w.layers * w.Hv * w.dk * w.dv
+
+
+TC_MAX_NODES = 32   # the tensor-core UT kernel takes d_v = 128 and n_max <= 32 (gdn_tree_verify's dispatch)
+
+
+def tc_applies(w: S.Workload) -> bool:
+    return w.dv == 128 and w.dk in (32, 64, 128) and w.n_max <= TC_MAX_NODES
+
+
+def tensor_flops(w: S.Workload, n_per_req):
+    """tf32 tensor-core FLOPs of the tensor-core UT kernel: per head T0^T [k | q] (M = d_v, N = 2 NB,
+    K = d_k) and the Gram rows (M = 128, N = NG, K = d_k), each split three ways (hi*hi + hi*lo + lo*hi);
+    NB = n rounded up to 8, NG = NB rounded up to 16."""
+    total = 0
+    for n in n_per_req:
+        nb = (n + 7) // 8 * 8
+        ng = (nb + 15) // 16 * 16
+        total += 3 * 2 * w.dk * (w.dv * 2 * nb + 128 * ng)
+    return total * w.layers * w.Hv
 
 
 def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
@@ -344,7 +373,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
             dist.barrier()
 
     # bytes / units of each step (pending length of step s = accepted path length of step s-1)
-    units_per_step, bytes_per_step, fma_per_step, walks = [], [], [], []
+    units_per_step, bytes_per_step, fma_per_step, tflops_per_step, walks = [], [], [], [], []
     for i in range(args.warmup + args.steps):
         s = i % w.steps
         n_req = [len(p) for p in plan.trees[s]]
@@ -360,7 +389,12 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
             ups = [int((np.bincount(p[1:], minlength=len(p)) > 0).sum()) if len(p) > 1 else 0 for p in plan.trees[s]]
         else:      # the tree-masked UT form applies no per-node update to the tile
             ups = [0] * w.B
-        fma_per_step.append(algorithmic_fma(w, n_req, ups, L_req))
+        if not walk and tc_applies(w):   # T0^T k and T0^T q on the tensor cores: the fold stays on FP32
+            fma_per_step.append(algorithmic_fma(w, [0] * w.B, ups, L_req))
+            tflops_per_step.append(tensor_flops(w, n_req))
+        else:
+            fma_per_step.append(algorithmic_fma(w, n_req, ups, L_req))
+            tflops_per_step.append(0)
 
     for i in range(args.warmup):
         one_step(i)
@@ -397,10 +431,12 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
 
     # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
     # A/B: the same steps with per-node-state schedules (every node reloads its parent's stored state)
-    ab = walk = None
+    ab = walk = simt = None
     if not args.no_ab:
-        walk = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node=False)
-        ab = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node=True)
+        if tc_applies(w) and not any(walks[args.warmup:]):
+            simt = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="ut_simt")
+        walk = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="walk")
+        ab = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="per_node")
 
     if args.no_e2e:
         e2e = dict(ms=float("nan"), units=0, steps=0, h2d=0, d2h=0)
@@ -415,39 +451,43 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     avg_bytes = statistics.mean(timed_bytes)
     achieved = avg_bytes / avg_verify_s / 1e9
     avg_flops = 2 * statistics.mean(fma_per_step[args.warmup:])
+    avg_tflops = statistics.mean(tflops_per_step[args.warmup:])
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
                                 (clk or {}).get("sm_max_mhz") or 2070.0)
     return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab, walk=walk,
+                simt=simt, avg_tflops=avg_tflops,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap, walked=any(walks[args.warmup:]),
                 gpu_launches=args.steps * 3)
 
 
-def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node):
-    """The same workload verified by walking a schedule instead of the tree-masked UT form: the
-    heavy-light chains (branch states in tensor memory), or -- per_node -- the per-node-state baseline,
-    whose schedule has no heavy edges so every node with children is stored to and reloaded from HBM
-    (the snapshot-style traffic the heavy-light chains avoid)."""
+def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode):
+    """The same workload verified another way: "walk" walks the heavy-light chains (branch states in
+    tensor memory); "per_node" walks the per-node-state baseline, whose schedule has no heavy edges so
+    every node with children is stored to and reloaded from HBM (the snapshot-style traffic the
+    heavy-light chains avoid); "ut_simt" solves the tree-masked UT form on the CUDA cores."""
     import torch
     from gated_deltanet_tree_gb300 import _native as N
+    per_node = mode == "per_node"
     steps = max(2, min(args.steps, 10))
-    packed, nb_cap = [], 1
+    packed, nb_cap, depth = [], 1, []
     for s in range(w.steps):
         P, n = parents_host[s]
-        words, nb = (N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules)(P, n)
+        words, nb, dm = (N.gdn_pack_schedules_per_node if per_node else N.gdn_pack_schedules)(P, n, with_depth=True)
         packed.append(torch.from_numpy(words).to(dev))
         nb_cap = max(nb_cap, nb)
+        depth.append(dm)
+    flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | (N.GDN_VERIFY_UT_SIMT if mode == "ut_simt" else N.GDN_VERIFY_CHAIN_WALK)
     boundary = torch.empty(w.B, w.layers, nb_cap, w.Hv, w.dk, w.dv, dtype=torch.float32, device=dev)
     ver = gs.ver
 
     def one(i):
         s = i % w.steps
-        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=nb_cap, words=packed[s].data_ptr())
+        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=nb_cap, depth_max=depth[s], words=packed[s].data_ptr())
         X, BE, AG = gs.inputs[s]
         N.gdn_tree_verify(gs.dims, w.layers, sc, X, gs.conv_w, BE, AG, gs.state, gs.conv_state, gs.out_o,
-                          boundary, ver.banks, ver.workspace, ver.ws_bytes,
-                          N.GDN_VERIFY_BOUNDARY_SCRATCH | N.GDN_VERIFY_CHAIN_WALK, stream)
+                          boundary, ver.banks, ver.workspace, ver.ws_bytes, flags, stream)
         N.gdn_commit_fold(gs.dims, w.layers, sc, paths[s][0], paths[s][1], 0, ver.banks, stream)
 
     for i in range(3):
@@ -465,8 +505,10 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, per_node):
     ms = e0.elapsed_time(e1)
     del boundary
     torch.cuda.empty_cache()
-    return {"schedule": "per-node states in HBM (no heavy edges)" if per_node else
-            "heavy-light chain walk, branch states in tensor memory", "steps": steps, "nb_max": nb_cap,
+    return {"schedule": {"per_node": "per-node states in HBM (no heavy edges)",
+                         "walk": "heavy-light chain walk, branch states in tensor memory",
+                         "ut_simt": "tree-masked UT form on the CUDA cores (ut_verify_kernel)"}[mode],
+            "steps": steps, "nb_max": nb_cap,
             "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
 
@@ -616,7 +658,8 @@ def main():
         "roofline": {"bound": "hbm" if r["avg_bytes"] / (r["peak"] * 1e9) >= r["avg_flops"] / (r["alu_peak"] * 1e12)
                      else "alu",
                      "kernel": "gdn_tree_verify (conv_window_kernel + "
-                               + ("chain_verify_kernel)" if r["walked"] else "ut_verify_kernel)"),
+                               + ("chain_verify_kernel)" if r["walked"] else
+                                  "ut_tc_verify_kernel)" if tc_applies(w) else "ut_verify_kernel)"),
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
@@ -625,7 +668,12 @@ def main():
                      "alu": {"achieved": r["avg_flops"] / r["avg_verify_s"] / 1e12, "peak": r["alu_peak"],
                              "unit": "TFLOP/s", "frac": r["avg_flops"] / r["avg_verify_s"] / 1e12 / r["alu_peak"],
                              "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x max SM clock",
-                             "algorithmic_flops_per_launch": r["avg_flops"]}},
+                             "algorithmic_flops_per_launch": r["avg_flops"]},
+                     "tensor": None if not r["avg_tflops"] else {
+                             "achieved": r["avg_tflops"] / r["avg_verify_s"] / 1e12, "peak": tf32_peak(),
+                             "unit": "TFLOP/s", "frac": r["avg_tflops"] / r["avg_verify_s"] / 1e12 / tf32_peak(),
+                             "peak_kind": "measured bf16 burst x 1/2 (nominal tf32 : bf16)",
+                             "tf32_flops_per_launch": r["avg_tflops"]}},
         "finish_ms": r["finish_ms"],
         "clocks": r["clocks"],
         "e2e": None if args.no_e2e else {
@@ -634,6 +682,8 @@ def main():
             "host_per_step": ("DDTree construction from the draft tables, " if w.tree == "ddtree" else "")
                              + "heavy-light schedules, packing"},
         "gpu_launches": r["gpu_launches"],
+        "ab_ut_simt": None if r["simt"] is None else dict(
+            r["simt"], tc_speedup=r["simt"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_chain_walk": None if r["walk"] is None else dict(
             r["walk"], ut_speedup=r["walk"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_per_node_states": None if r["ab"] is None else dict(

@@ -33,6 +33,7 @@ GDN_DTYPE_BF16 = 1
 GDN_COMMIT_COMPACT = 1
 GDN_VERIFY_BOUNDARY_SCRATCH = 1
 GDN_VERIFY_CHAIN_WALK = 2
+GDN_VERIFY_UT_SIMT = 4
 GDN_MAX_NODES = 64
 
 

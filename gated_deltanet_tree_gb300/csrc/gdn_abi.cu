@@ -149,7 +149,7 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
                            float* conv_state, float* out_o, float* boundary_states, gdn_banks* banks,
                            void* workspace, size_t workspace_bytes, int32_t flags, cudaStream_t stream) {
   gdn::clear_error();
-  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK))
+  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT))
     return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
   GDN_TRY(check_dims(d));
   GDN_TRY(check_sched(sched));
@@ -205,8 +205,16 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];
   }
   vp.pend_path = banks->pend_path; vp.pend_len = banks->pend_len; vp.err = banks->err;
-  e = vp.chain_walk ? gdn::launch_verify(vp, stream) : gdn::launch_verify_ut(vp, stream);
-  if (e != cudaSuccess) return cuda_fail(e, vp.chain_walk ? "chain-verify launch" : "tree-verify launch");
+  if (vp.chain_walk) {
+    e = gdn::launch_verify(vp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "chain-verify launch");
+  } else if (!(flags & GDN_VERIFY_UT_SIMT) && gdn::verify_tc_supported(d->dk, d->dv, n_max)) {
+    e = gdn::launch_verify_tc(vp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores)");
+  } else {
+    e = gdn::launch_verify_ut(vp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch");
+  }
 
   banks->pend_bank = -1;
   banks->verified_bank = cur;

@@ -144,6 +144,57 @@ struct RegTile {
   }
 };
 
+// One column of a [d_k][d_v] state, NR consecutive rows of it, as packed (row r, row r + 1) pairs:
+// T[j] = (T[row0 + 2j][c], T[row0 + 2j + 1][c]).  The element operations are those of RegTile
+// (same operands, same order), so a state folded in one layout equals, bit for bit, the state
+// folded or stored in the other.  Pointers point at the thread's first element; `ld` is the row
+// stride in floats.
+template <int NR>
+struct ColTile {
+  static constexpr int NP = NR / 2;
+  u64 T[NP];
+
+  __device__ __forceinline__ void load(const float* base, size_t ld) {
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+      T[j] = pack2(base[static_cast<size_t>(2 * j) * ld], base[static_cast<size_t>(2 * j + 1) * ld]);
+  }
+  __device__ __forceinline__ void store(float* base, size_t ld) const {
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      const float2 a = unpack2(T[j]);
+      base[static_cast<size_t>(2 * j) * ld] = a.x;
+      base[static_cast<size_t>(2 * j + 1) * ld] = a.y;
+    }
+  }
+  __device__ __forceinline__ void materialise(float gam) {
+    const u64 g2 = pack2(gam, gam);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) T[j] = mul2(g2, T[j]);
+  }
+  // T <- fmaf(k, ut, T); krows = k + row0 (16-byte aligned; shared or global memory)
+  __device__ __forceinline__ void update_lazy(const float* krows, float ut) {
+    const u64 u2 = pack2(ut, ut);
+    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(krows);
+#pragma unroll
+    for (int j4 = 0; j4 < NP / 2; ++j4) {
+      const ulonglong2 kk = k4[j4];
+      T[2 * j4 + 0] = fma2(kk.x, u2, T[2 * j4 + 0]);
+      T[2 * j4 + 1] = fma2(kk.y, u2, T[2 * j4 + 1]);
+    }
+  }
+  // RegTile::advance for one column
+  __device__ __forceinline__ float advance(const float* krows, float gam1, float u) {
+    if (gam1 < kGammaFloor) {
+      materialise(gam1);
+      gam1 = 1.f;
+    }
+    const float r = __fdividef(1.f, gam1);
+    update_lazy(krows, u * r);
+    return gam1;
+  }
+};
+
 // The four column sums of packed (even, odd) partials.
 __device__ __forceinline__ float4 fold_pairs(const u64 (&a)[kCols]) {
   const float2 a0 = unpack2(a[0]), a1 = unpack2(a[1]), a2 = unpack2(a[2]), a3 = unpack2(a[3]);

@@ -52,88 +52,12 @@
 #include <type_traits>
 
 #include "gdn_tile.cuh"
+#include "gdn_umma.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kVerifyThreads = 128;
-
-// ---- tensor memory (tcgen05) as a stash for register tiles: the 32x32b access shape gives each
-// thread of a warp its own lane, so a tile held in registers moves in and out without crossing lanes.
-__host__ __device__ constexpr uint32_t tmem_columns(int words) {   // allocation: a power of two >= 32, or none
-  return words <= 0 ? 0u : words <= 32 ? 32u : words <= 64 ? 64u : words <= 128 ? 128u : words <= 256 ? 256u : 512u;
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(cols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
-}
-__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// Loads 32 words of this thread's lane into 16 packed pairs; the wait is inside, so the
-// outputs are defined when the statement ends.
-__device__ __forceinline__ void tmem_get32(uint32_t ta, u64 (&v)[16]) {
-  asm volatile(
-      "{\n"
-      " .reg .b32 t<32>;\n"
-      " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%16];\n"
-      " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%17];\n"
-      " tcgen05.wait::ld.sync.aligned;\n"
-      " mov.b64 %0, {t0, t1};\n"
-      " mov.b64 %1, {t2, t3};\n"
-      " mov.b64 %2, {t4, t5};\n"
-      " mov.b64 %3, {t6, t7};\n"
-      " mov.b64 %4, {t8, t9};\n"
-      " mov.b64 %5, {t10, t11};\n"
-      " mov.b64 %6, {t12, t13};\n"
-      " mov.b64 %7, {t14, t15};\n"
-      " mov.b64 %8, {t16, t17};\n"
-      " mov.b64 %9, {t18, t19};\n"
-      " mov.b64 %10, {t20, t21};\n"
-      " mov.b64 %11, {t22, t23};\n"
-      " mov.b64 %12, {t24, t25};\n"
-      " mov.b64 %13, {t26, t27};\n"
-      " mov.b64 %14, {t28, t29};\n"
-      " mov.b64 %15, {t30, t31};\n"
-      "}"
-      : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3]), "=l"(v[4]), "=l"(v[5]), "=l"(v[6]), "=l"(v[7]), "=l"(v[8]), "=l"(v[9]), "=l"(v[10]), "=l"(v[11]), "=l"(v[12]), "=l"(v[13]), "=l"(v[14]), "=l"(v[15])
-      : "r"(ta + 0u), "r"(ta + 16u)
-      : "memory");
-}
-// Stores 16 packed pairs as 32 words of this thread's lane and waits for the stores.
-__device__ __forceinline__ void tmem_put32(uint32_t ta, const u64 (&v)[16]) {
-  asm volatile(
-      "{\n"
-      " .reg .b32 t<32>;\n"
-      " mov.b64 {t0, t1}, %0;\n"
-      " mov.b64 {t2, t3}, %1;\n"
-      " mov.b64 {t4, t5}, %2;\n"
-      " mov.b64 {t6, t7}, %3;\n"
-      " mov.b64 {t8, t9}, %4;\n"
-      " mov.b64 {t10, t11}, %5;\n"
-      " mov.b64 {t12, t13}, %6;\n"
-      " mov.b64 {t14, t15}, %7;\n"
-      " mov.b64 {t16, t17}, %8;\n"
-      " mov.b64 {t18, t19}, %9;\n"
-      " mov.b64 {t20, t21}, %10;\n"
-      " mov.b64 {t22, t23}, %11;\n"
-      " mov.b64 {t24, t25}, %12;\n"
-      " mov.b64 {t26, t27}, %13;\n"
-      " mov.b64 {t28, t29}, %14;\n"
-      " mov.b64 {t30, t31}, %15;\n"
-      " tcgen05.st.sync.aligned.32x32b.x16.b32 [%16], {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15};\n"
-      " tcgen05.st.sync.aligned.32x32b.x16.b32 [%17], {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31};\n"
-      " tcgen05.wait::st.sync.aligned;\n"
-      "}"
-      :
-      : "l"(v[0]), "l"(v[1]), "l"(v[2]), "l"(v[3]), "l"(v[4]), "l"(v[5]), "l"(v[6]), "l"(v[7]), "l"(v[8]), "l"(v[9]), "l"(v[10]), "l"(v[11]), "l"(v[12]), "l"(v[13]), "l"(v[14]), "l"(v[15]), "r"(ta + 0u), "r"(ta + 16u)
-      : "memory");
-}
 
 // Shared-memory layout (floats): tree region, fold region, then the schedule record (int32).
 template <int DK>

@@ -241,6 +241,7 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
 
 #define GDN_VERIFY_BOUNDARY_SCRATCH 1   /* boundary_states is scratch, not output */
 #define GDN_VERIFY_CHAIN_WALK 2         /* walk the heavy-light chains instead of the tree-masked UT form */
+#define GDN_VERIFY_UT_SIMT 4            /* UT form on the CUDA cores even where the tensor-core kernel applies */
 
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify -- fold the pending path, then verify a batch of trees.
@@ -266,15 +267,18 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              With GDN_VERIFY_BOUNDARY_SCRATCH in flags it is scratch instead: only
  *              stashes that spill out of tensor memory are written there, and its
  *              contents are unspecified on return.
- *   flags      GDN_VERIFY_BOUNDARY_SCRATCH and/or GDN_VERIFY_CHAIN_WALK (other bits:
- *              GDN_ERR_INVALID_ARG).  By default the nodes are solved in the tree-masked
- *              UT form (article "状态驻留验证": the topology-masked UT decomposition): one
- *              sweep of the committed state per node, no dependency between nodes, then a
- *              forward substitution over ancestor pairs.  GDN_VERIFY_CHAIN_WALK walks the
- *              packed ops instead: heavy-light chains in registers, branch states stashed in
- *              tensor memory.  Both give the same results up to rounding.  Batches whose
- *              sched->depth_max exceeds GDN_UT_MAX_DEPTH walk chains without the flag: the
- *              UT form's per-node work grows with the square of the depth.
+ *   flags      GDN_VERIFY_BOUNDARY_SCRATCH, GDN_VERIFY_CHAIN_WALK, GDN_VERIFY_UT_SIMT (other
+ *              bits: GDN_ERR_INVALID_ARG).  By default the nodes are solved in the tree-masked
+ *              UT form (article "状态驻留验证": the topology-masked UT decomposition): the
+ *              committed state times every node's k and q, with no dependency between nodes,
+ *              then a substitution over ancestor pairs.  Where dv = 128 and n_max <= 32 those
+ *              products and the nodes' Gram rows run on the tensor cores (tcgen05, tf32 split
+ *              in three for fp32 accuracy); elsewhere, or with GDN_VERIFY_UT_SIMT, on the CUDA
+ *              cores.  GDN_VERIFY_CHAIN_WALK walks the packed ops instead: heavy-light chains
+ *              in registers, branch states stashed in tensor memory.  All give the same results
+ *              up to rounding.  Batches whose sched->depth_max exceeds GDN_UT_MAX_DEPTH walk
+ *              chains without the flag: the UT form's per-node work grows with the square of
+ *              the depth.
  *   banks      factors of every node are written into bank write_bank
  *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
  * Rows of nodes >= n[b] are neither read nor written.

@@ -27,15 +27,26 @@ def _np(t):
     return t.detach().cpu().numpy().astype(np.float64)
 
 
-def run_parity(w, units=None, compact_steps=(), finish=True, plan=None, layer_ids=None, chain_walk=False):
+# verify kernels: "ut" the default dispatch (the tree-masked UT form, on the tensor cores where d_v = 128
+# and n_max <= 32), "simt" the UT form on the CUDA cores, "walk" the heavy-light chain walk
+KERNELS = ["ut", "simt", "walk"]
+
+
+def set_kernel(plan, kernel):
+    assert kernel in KERNELS, kernel
+    plan.chain_walk = plan.chain_walk or kernel == "walk"
+    plan.ut_simt = plan.ut_simt or kernel == "simt"
+    return plan
+
+
+def run_parity(w, units=None, compact_steps=(), finish=True, plan=None, layer_ids=None, kernel="ut"):
     """Run every step of workload w on the GPU; compare the chosen units with the oracle.
 
     layer_ids: the layers one call covers (a layer chunk); units must lie in it.
-    chain_walk: verify by walking the heavy-light chains instead of the tree-masked UT form.
+    kernel: which verify kernel runs (KERNELS).
     """
     from harness import GpuSession, WorkloadPlan
-    plan = plan or WorkloadPlan(w)
-    plan.chain_walk = plan.chain_walk or chain_walk
+    plan = set_kernel(plan or WorkloadPlan(w), kernel)
     gs = GpuSession(w, plan, layer_ids=layer_ids)
     if units is None:
         units = [(b, l) for b in range(w.B) for l in gs.layer_ids]
@@ -93,10 +104,10 @@ def run_parity(w, units=None, compact_steps=(), finish=True, plan=None, layer_id
 # small cases, every element
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_tiny_conv_mode(chain_walk):
+@pytest.mark.parametrize("kernel", ["ut", "walk"])
+def test_tiny_conv_mode(kernel):
     w = S.workload(1).replace(steps=4)
-    run_parity(w, chain_walk=chain_walk)
+    run_parity(w, kernel=kernel)
 
 
 def test_tiny_bypass_mode():
@@ -104,19 +115,27 @@ def test_tiny_bypass_mode():
     run_parity(w)
 
 
-@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 32), (128, 32), (64, 128), (128, 128), (32, 32)])
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_head_shapes_and_gqa(dk, dv, chain_walk):
+@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 32), (128, 32), (32, 128), (64, 128), (128, 128), (32, 32)])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_head_shapes_and_gqa(dk, dv, kernel):
     # d_k != d_v catches a transposed state; Hv = 3 Hk checks the v-head -> k-head map
+    if kernel == "simt" and dv != 128:
+        pytest.skip("the default UT dispatch already runs the CUDA-core kernel for this d_v")
     w = S.workload(1).replace(Hk=2, Hv=6, dk=dk, dv=dv, steps=3, tree="random", budget=12, n_max=12, path_max=12)
-    run_parity(w, chain_walk=chain_walk)
+    run_parity(w, kernel=kernel)
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_ragged_batch_and_degenerate_trees(chain_walk):
-    # per-request tree sizes 1 .. n_max, a single-node tree, a full chain, L = 0 and L = n commits
-    n_max = 16
+@pytest.mark.parametrize("heads", ["tiny", "d128"])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_ragged_batch_and_degenerate_trees(heads, kernel):
+    # per-request tree sizes 1 .. n_max, a single-node tree, a full chain, L = 0 and L = n commits;
+    # with 128-wide heads the UT form runs on the tensor cores, whose node padding these sizes cross
+    n_max = 16 if heads == "tiny" else 32
+    if heads == "tiny" and kernel == "simt":
+        pytest.skip("the default UT dispatch already runs the CUDA-core kernel for these heads")
     w = S.workload(1).replace(B=5, layers=2, n_max=n_max, steps=3, tree="random", budget=n_max, path_max=n_max)
+    if heads == "d128":
+        w = w.replace(Hk=2, Hv=6, dk=128, dv=128)
     rng = np.random.default_rng(5)
     trees, paths = [], []
     for s in range(w.steps):
@@ -127,7 +146,7 @@ def test_ragged_batch_and_degenerate_trees(chain_walk):
         trees.append(ts)
         paths.append(ps)
     from harness import WorkloadPlan
-    run_parity(w, plan=WorkloadPlan(w, trees, paths), chain_walk=chain_walk)
+    run_parity(w, plan=WorkloadPlan(w, trees, paths), kernel=kernel)
 
 
 def test_compaction_is_exact_and_transparent():
@@ -149,8 +168,8 @@ def binary_tree(n):
 
 
 @pytest.mark.parametrize("cfg", [1, 2], ids=["tiny", "qwen"])
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_deep_light_depth_spills_stashes_to_hbm(cfg, chain_walk):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_deep_light_depth_spills_stashes_to_hbm(cfg, kernel):
     # perfect binary trees (light depth 4 at 31 nodes) and random 32-node trees: stashes two or more
     # levels deep leave tensor memory for the boundary slots, and every node must still match
     from harness import WorkloadPlan
@@ -163,11 +182,13 @@ def test_deep_light_depth_spills_stashes_to_hbm(cfg, chain_walk):
         ts = [binary_tree(31), binary_tree(n_max), S.random_tree(n_max, rng)]
         trees.append(ts)
         paths.append([S.random_walk_path(t, rng, max_len=n_max) for t in ts])
-    run_parity(w, plan=WorkloadPlan(w, trees, paths), chain_walk=chain_walk)
+    if cfg == 1 and kernel == "simt":
+        pytest.skip("the default UT dispatch already runs the CUDA-core kernel for these heads")
+    run_parity(w, plan=WorkloadPlan(w, trees, paths), kernel=kernel)
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_boundary_scratch_changes_no_result(chain_walk):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_boundary_scratch_changes_no_result(kernel):
     # with boundary states as scratch the outputs, banks and committed states are bit-identical
     from harness import GpuSession, WorkloadPlan
     n_max = 32
@@ -175,7 +196,7 @@ def test_boundary_scratch_changes_no_result(chain_walk):
     rng = np.random.default_rng(23)
     trees = [[binary_tree(31), S.ddtree(22, 4, 10, rng), S.random_tree(n_max, rng)] for _ in range(w.steps)]
     paths = [[S.random_walk_path(t, rng, max_len=n_max) for t in ts] for ts in trees]
-    plan = WorkloadPlan(w, trees, paths, chain_walk=chain_walk)
+    plan = set_kernel(WorkloadPlan(w, trees, paths), kernel)
     a, b = GpuSession(w, plan), GpuSession(w, plan)
     for s in range(w.steps):
         a.verify(s)
@@ -196,27 +217,27 @@ def test_boundary_scratch_changes_no_result(chain_walk):
     b.ver.check_error()
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_qwen_like_single_layer(chain_walk):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_qwen_like_single_layer(kernel):
     w = S.workload(2).replace(steps=3)
-    run_parity(w, chain_walk=chain_walk)
+    run_parity(w, kernel=kernel)
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_chain64_single_layer(chain_walk):
+@pytest.mark.parametrize("kernel", ["ut", "walk"])
+def test_chain64_single_layer(kernel):
     # the pure-chain shape of the stress workload: 64-node chain, chain acceptance of the whole walk
     # the UT form would hand a 63-deep chain to the walk; here it is made to solve it itself
     from harness import WorkloadPlan
     w = S.workload(6).replace(B=2, layers=1, steps=2)
     plan = WorkloadPlan(w)
-    plan.depth_hint = chain_walk
-    run_parity(w, plan=plan, chain_walk=chain_walk)
+    plan.depth_hint = kernel == "walk"
+    run_parity(w, plan=plan, kernel=kernel)
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_ddtree64_top8_single_layer(chain_walk):
+@pytest.mark.parametrize("kernel", ["ut", "walk"])
+def test_ddtree64_top8_single_layer(kernel):
     w = S.workload(5).replace(B=2, layers=1, steps=2)
-    run_parity(w, chain_walk=chain_walk)
+    run_parity(w, kernel=kernel)
 
 
 # ---------------------------------------------------------------------------
@@ -228,10 +249,10 @@ def test_qwen_48_layers_commit_then_verify():
     run_parity(w, units=[(0, 0), (0, 17), (0, 47)])
 
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_batched_32x48_eight_steps(chain_walk):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_batched_32x48_eight_steps(kernel):
     w = S.workload(4)
-    run_parity(w, units=[(0, 0), (13, 29), (31, 47)], chain_walk=chain_walk)
+    run_parity(w, units=[(0, 0), (13, 29), (31, 47)], kernel=kernel)
 
 
 @pytest.mark.parametrize("cfg", [5, 6], ids=["ddtree64_top8", "chain64"])
@@ -285,8 +306,8 @@ def test_checkpoint_resume_is_bitwise():
 # lifecycle and device-side checks
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("chain_walk", [False, True], ids=["ut", "walk"])
-def test_fold_reproduces_boundary_state_bitwise(chain_walk):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_fold_reproduces_boundary_state_bitwise(kernel):
     """The committed state folded from the factor bank equals, bit for bit, the
     state the previous verify stored for the path's last node when that node was
     a boundary (same operation order in fold and verify)."""
@@ -300,7 +321,7 @@ def test_fold_reproduces_boundary_state_bitwise(chain_walk):
     while p0[path[-1]] >= 0:
         path.append(int(p0[path[-1]]))
     plan.paths[0][0] = np.array(path[::-1], dtype=np.int32)
-    plan.chain_walk = chain_walk
+    set_kernel(plan, kernel)
     gs = GpuSession(w, plan)
     gs.verify(0)
     slot = sorted(i for i in range(len(p0)) if kids[i] >= 2).index(target)
