@@ -131,6 +131,7 @@ struct VerifyParams {
   const int32_t* pend_path;
   const int32_t* pend_len;
   int32_t* err;                // device error words
+  int prefetch_ahead;          // CTAs ahead whose inputs a CTA prefetches into L2 (0: none)
 };
 
 struct CommitParams {
