@@ -10,11 +10,12 @@
 // Nearly all the arithmetic is one product with no dependency between nodes,
 // T0^T [k_0 .. k_{n-1} q_0 .. q_{n-1}] (d_v x d_k times d_k x 2n per head).  It
 // runs here as tcgen05 MMAs of kind tf32 split three ways, A_hi B_hi + A_hi B_lo
-// + A_lo B_hi, so that it carries fp32 accuracy.  The Gram coefficients are only
-// needed for ancestor pairs (about n * depth of them); they are fp32 dot products
-// on the CUDA cores while the tensor cores run.  What follows (the
-// ancestor-pattern inverse M = (I + A)^-1 and the sums over ancestors) is the
-// CUDA-core UT kernel's.
+// + A_lo B_hi, so that it carries fp32 accuracy; so do the Gram rows [k; q] k^T,
+// issued before the fold and read out of tensor memory after it.  The tree's
+// tables (depths, pair offsets, ancestors, rho and Gamma by a product scan
+// across lanes, the pair coefficients, the rows of M = (I + A)^-1) are built by
+// warps or threads in parallel while the tensor cores run; u and o are the
+// sums over ancestors of the CUDA-core UT kernel.
 //
 // Work unit: one CTA per (request, layer, v-head), 256 threads, d_v = 128.
 // Thread (warp w, lane) owns column c = 32 (w % 4) + lane of the [d_k][d_v]
@@ -27,11 +28,15 @@
 //   [0, d_k)           A = T0^T: first its tf32 high part, then, once the MMAs
 //                      reading it completed, its low part
 //   [128, 128 + 4 NB)  D: columns t, NB + t, 2 NB + t, 3 NB + t hold T0^T times
-//                      the high k_t, high q_t, low k_t and low q_t
+//                      the high k_t, high q_t, low k_t and low q_t; before the
+//                      first product, the Gram rows
 // with NB = n rounded up to 8.  The first product (A high, N = 4 NB) fills all
 // four blocks; the second (A low times the high rows, N = 2 NB) accumulates into
 // the first two, so T0^T k_t = D[t] + D[2 NB + t] and T0^T q_t = D[NB + t] +
-// D[3 NB + t].
+// D[3 NB + t].  The Gram rows are the operand's first 128 rows (k_hi, q_hi,
+// k_lo, q_lo, then rows never read out) times the high k rows and times the low
+// k rows (N = NB rounded up to 16 each), so G_ts and H_ts are each a sum of
+// three lanes.
 //
 // Shared-memory operand: rows k_hi | q_hi | k_lo | q_lo (NB rows each, rows of
 // nodes >= n zero), K-major without swizzle, chunk-major: the 16-byte chunk kc
