@@ -145,16 +145,21 @@ def tc_applies(w: S.Workload) -> bool:
     return w.dv == 128 and w.dk in (32, 64, 128) and w.n_max <= TC_MAX_NODES
 
 
+def tc_mma_shapes(w: S.Workload, n: int):
+    """(M, N, K) of every tcgen05 MMA the tensor-core UT kernel issues for one head and a tree of n nodes
+    (NB = n rounded up to 8, NG = NB rounded up to 16; K = 8 per instruction, d_k / 8 instructions each):
+    the Gram rows (the operand's 128 rows times the high and times the low k rows), T0^T_hi times all
+    4 NB rows (high and low k, q), T0^T_lo times the 2 NB high rows."""
+    nb = (n + 7) // 8 * 8
+    ng = (nb + 15) // 16 * 16
+    per_step = [(128, ng, 8), (128, ng, 8), (w.dv, 4 * nb, 8), (w.dv, 2 * nb, 8)]
+    return per_step * (w.dk // 8)
+
+
 def tensor_flops(w: S.Workload, n_per_req):
-    """tf32 tensor-core FLOPs of the tensor-core UT kernel: per head T0^T [k | q] (M = d_v, N = 2 NB,
-    K = d_k) and the Gram rows (M = 128, N = NG, K = d_k), each split three ways (hi*hi + hi*lo + lo*hi);
-    NB = n rounded up to 8, NG = NB rounded up to 16."""
-    total = 0
-    for n in n_per_req:
-        nb = (n + 7) // 8 * 8
-        ng = (nb + 15) // 16 * 16
-        total += 3 * 2 * w.dk * (w.dv * 2 * nb + 128 * ng)
-    return total * w.layers * w.Hv
+    """tf32 FLOPs the tensor cores execute in one verify call (2 M N K per MMA)."""
+    per_head = sum(sum(2 * m * nn * k for m, nn, k in tc_mma_shapes(w, n)) for n in n_per_req)
+    return per_head * w.layers * w.Hv
 
 
 def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:

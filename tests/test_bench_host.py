@@ -90,3 +90,16 @@ def test_hbm_stashes_counts_spilled_pushes():
     assert bench.hbm_stashes(words, n_max) == [spilled]
     assert bench.hbm_stashes(N.gdn_pack_schedules_per_node(P, np.array([len(parent)], dtype=np.int32))[0],
                              n_max) == [int((np.bincount(parent[1:], minlength=len(parent)) > 0).sum())]
+
+
+def test_tensor_core_flops_follow_the_issued_mmas():
+    """One head, one layer: the tf32 FLOPs reported are those of the MMAs the kernel issues (two Gram
+    MMAs, one N = 4 NB and one N = 2 NB product per K step of 8), and the kernel applies where the
+    dispatch sends batches to it."""
+    import bench
+    w = S.workload(2).replace(Hk=1, Hv=1, layers=1, B=1)
+    shapes = bench.tc_mma_shapes(w, 22)
+    assert len(shapes) == 4 * 128 // 8
+    assert sorted({n for _, n, _ in shapes}) == [32, 48, 96]   # NG, 2 NB, 4 NB for NB = 24
+    assert bench.tensor_flops(w, [22]) == 16 * 2 * 128 * 8 * (32 + 32 + 96 + 48)
+    assert bench.tc_applies(w) and not bench.tc_applies(w.replace(n_max=64)) and not bench.tc_applies(w.replace(dv=64))
