@@ -16,10 +16,13 @@
 //            write-back needs no barrier) and one thread per node records the
 //            node's K-1 nearest ancestors;
 //   phase 1: for every node convolve the window (tree ancestors, then the
-//            committed rows past the root), apply SiLU, keep y in shared
-//            memory and copy the raw row into the factor bank;
-//   phase 2: one warp per (node, head): sum of squares, normalise q and k,
-//            write q_hat / k_hat / v with 16-byte stores.
+//            committed rows past the root), apply SiLU, copy the raw row into
+//            the factor bank, normalise q and k over each head's channels (a
+//            segmented shuffle; a 128-channel head's two warps add their halves
+//            through shared memory) and write q_hat / k_hat / v at once.
+// Nothing per node stays in shared memory but the staged raw rows, so a CTA
+// needs ~12 KB and the SM's thread count, not its shared memory, bounds the
+// CTAs resident at once.
 // SiLU uses the fast exp and divide intrinsics (relative error ~1e-7).
 #include <cuda_bf16.h>
 
@@ -73,10 +76,9 @@ __device__ __forceinline__ HeadGroup head_group(const ConvParams& p, int y) {
 // registers); KT = 0 reads it from the parameters.
 template <typename InT, int KT>
 __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p) {
-  // shared: ybuf [n_max][256] f32 | xs [n_max][256] InT | anc [n_max][K-1] int32 | mbarrier
+  // shared: xs [n_max][256] InT | anc [n_max][K-1] int32 | mbarrier | partial sums [2][warps] f32
   extern __shared__ float4 smem_conv[];
-  float2* ybuf = reinterpret_cast<float2*>(smem_conv);
-  InT* xs = reinterpret_cast<InT*>(reinterpret_cast<char*>(smem_conv) + p.n_max * kConvChannels * 4);
+  InT* xs = reinterpret_cast<InT*>(smem_conv);
   int32_t* anc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(xs) + p.n_max * kConvChannels * sizeof(InT));
   uint64_t* bar = reinterpret_cast<uint64_t*>(anc + ((p.n_max * (GDN_MAX_TAPS - 1) + 3) & ~3));
   const int bl = blockIdx.x;                   // request * layers + layer
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p)
   const bool active = 2 * tid < width;
   const int K = KT > 0 ? KT : p.K, C = p.C;
   const InT* x = static_cast<const InT*>(p.x_raw);
-  if (launch_aborted(p.err)) return;
+  if (__syncthreads_or(launch_aborted(p.err))) return;   // an earlier CTA gave up on a wait (one verdict)
 
   const SchedLayout lay{p.n_max};
   const int32_t* rec = p.words ? p.words + static_cast<size_t>(b) * lay.words() : nullptr;
@@ -154,14 +156,34 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p)
 #pragma unroll
     for (int j = 0; j < K; ++j) w[j] = make_float2(cw[j], cw[K + j]);
   }
-  if (!mbar_wait(bar, 0)) {
+  if (!__syncthreads_and(mbar_wait(bar, 0))) {   // one verdict for the CTA; also publishes the ancestor table
     if (tid == 0) device_error(p.err, GDN_DEVERR_TIMEOUT, b);
-    mbar_wait(bar, 0);
+    mbar_wait(bar, 0);   // let the copies land before the CTA exits
     return;
   }
-  __syncthreads();   // ancestor table visible
 
-  // phase 1: conv + activation of every node
+  // per node: conv + activation, then (q and k heads) the L2 normalisation over the head's channels, and the
+  // outputs written at once.  A head's channels are hsz / 2 consecutive threads: a segmented shuffle sums
+  // their squares; a 128-channel head spans two warps, which add their halves through a shared slot
+  // (double-buffered by node parity, so one barrier per node suffices).
+  const int lane = tid & 31, warp = tid >> 5;
+  const int hthreads = hg.hsz / 2;                  // threads per head
+  const int hh = (2 * tid) / hg.hsz;                // head within the group
+  const int e0 = 2 * tid - hh * hg.hsz;             // first channel within the head
+  float* part = reinterpret_cast<float*>(bar + 1);  // [2][kConvThreads / 32]
+  const int kind = hg.kind;
+  float* dst0 = nullptr;
+  size_t dst_row = 0;
+  if (kind == 0) {
+    dst0 = p.q_out + static_cast<size_t>(hg.head0 + hh) * p.dk + e0;
+    dst_row = static_cast<size_t>(p.Hk) * p.dk;
+  } else if (kind == 1) {
+    dst0 = p.k_out + static_cast<size_t>(hg.head0 + hh) * p.dk + e0;
+    dst_row = static_cast<size_t>(p.Hk) * p.dk;
+  } else {
+    dst0 = p.v_out + static_cast<size_t>(hg.head0 + hh) * p.dv + e0;
+    dst_row = static_cast<size_t>(p.Hv) * p.dv;
+  }
   for (int node = 0; node < n; ++node) {
     float2 y = make_float2(0.f, 0.f);
     if (active) {
@@ -196,34 +218,20 @@ __global__ void __launch_bounds__(kConvThreads) conv_window_kernel(ConvParams p)
         y.y = silu(y.y);
       }
     }
-    ybuf[node * kConvThreads + tid] = y;
-  }
-  __syncthreads();
-
-  // phase 2: one warp per (node, head) -- normalise q and k, write q_hat, k_hat, v
-  const int lane = tid & 31, warp = tid >> 5;
-  const float* yb = reinterpret_cast<const float*>(ybuf);
-  const int kind = hg.kind, hsz = hg.hsz, head0 = hg.head0, heads = hg.heads;
-  for (int job = warp; job < n * heads; job += kConvThreads / 32) {
-    const int node = job / heads, hh = job % heads;
-    const float* yh = yb + node * kConvChannels + hh * hsz;
     float scale = 1.f;
-    if (kind < 2) {
-      float ss = 0.f;
-      for (int e = lane; e < hsz; e += 32) ss = fmaf(yh[e], yh[e], ss);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (kind < 2) {   // CTA-uniform
+      float ss = fmaf(y.x, y.x, y.y * y.y);
+      for (int o = (hthreads < 32 ? hthreads : 32) / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (hthreads > 32) {   // two warps per head
+        if (lane == 0) part[(node & 1) * (kConvThreads / 32) + warp] = ss;
+        __syncthreads();
+        ss += part[(node & 1) * (kConvThreads / 32) + (warp ^ 1)];
+      }
       scale = 1.f / sqrtf(ss + p.l2_eps);
       if (kind == 0) scale *= p.q_scale;
     }
-    float* dst;
-    if (kind == 0) dst = p.q_out + ((xrow0 + node) * p.Hk + head0 + hh) * p.dk;
-    else if (kind == 1) dst = p.k_out + ((xrow0 + node) * p.Hk + head0 + hh) * p.dk;
-    else dst = p.v_out + ((xrow0 + node) * p.Hv + head0 + hh) * p.dv;
-    for (int e = 4 * lane; e < hsz; e += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(yh + e);
-      *reinterpret_cast<float4*>(dst + e) = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
-    }
+    if (active)
+      *reinterpret_cast<float2*>(dst0 + (xrow0 + node) * dst_row) = make_float2(y.x * scale, y.y * scale);
   }
 }
 
@@ -232,8 +240,8 @@ cudaError_t launch_t(const ConvParams& p, cudaStream_t s) {
   const int hq = kConvChannels / p.dk, hv = kConvChannels / p.dv;
   dim3 grid(p.B * p.layers, 2 * ((p.Hk + hq - 1) / hq) + (p.Hv + hv - 1) / hv);
   const size_t smem =
-      p.words ? static_cast<size_t>(p.n_max) * kConvChannels * (4 + sizeof(InT)) +
-                    ((p.n_max * (GDN_MAX_TAPS - 1) + 3) & ~3) * 4 + 16
+      p.words ? static_cast<size_t>(p.n_max) * kConvChannels * sizeof(InT) +
+                    ((p.n_max * (GDN_MAX_TAPS - 1) + 3) & ~3) * 4 + 16 + 2 * (kConvThreads / 32) * 4
               : 0;
   auto k = conv_window_kernel<InT, KT>;
   if (smem > 48 * 1024) {
