@@ -326,6 +326,60 @@ def test_every_tree_matches_ut_form(n):
                 np.testing.assert_allclose(res["boundary"][s, h], Ts[b], atol=1e-12)
 
 
+def _chunked_chain_form(T0, q, k, v, beta, g, C):
+    """Chunked UT/WY form of one head on a chain (independent of the per-node replay): the chain is cut
+    into chunks of C nodes; inside a chunk with start state Tj and gates accumulated from the chunk's
+    start (Gam), the residuals solve (I + A) U = beta (V - Gam K Tj) with A[t, s] = beta_t Gam_t / Gam_s
+    (k_t . k_s) for s < t in the chunk; o_t = Gam_t Tj^T q_t + sum_{s <= t} Gam_t / Gam_s (k_s . q_t) u_s;
+    the next chunk starts from Gam_end Tj + sum_s Gam_end / Gam_s k_s u_s^T (a rank-C update)."""
+    n = len(q)
+    T = T0.copy()
+    o = np.zeros((n, T0.shape[1]))
+    U = np.zeros((n, T0.shape[1]))
+    for c0 in range(0, n, C):
+        idx = np.arange(c0, min(n, c0 + C))
+        m = len(idx)
+        Gam = np.cumprod(g[idx])
+        A = np.zeros((m, m))
+        for t in range(m):
+            for s_ in range(t):
+                A[t, s_] = beta[idx[t]] * Gam[t] / Gam[s_] * (k[idx[t]] @ k[idx[s_]])
+        rhs = beta[idx, None] * (v[idx] - Gam[:, None] * (k[idx] @ T))
+        Uc = np.linalg.solve(np.eye(m) + A, rhs)
+        for t in range(m):
+            o[idx[t]] = Gam[t] * (T.T @ q[idx[t]])
+            for s_ in range(t + 1):
+                o[idx[t]] += Gam[t] / Gam[s_] * (k[idx[s_]] @ q[idx[t]]) * Uc[s_]
+        U[idx] = Uc
+        T = Gam[-1] * T + sum(Gam[-1] / Gam[s_] * np.outer(k[idx[s_]], Uc[s_]) for s_ in range(m))
+    return o, U, T
+
+
+@pytest.mark.parametrize("C", [1, 5, 16, 64])
+def test_chain_matches_chunked_ut_form(C):
+    # the long-chain stress shape: a 64-node chain, its outputs, residuals and end state against the
+    # chunked UT/WY form for chunk sizes that divide it and that leave a ragged last chunk
+    n = 64
+    d = O.Dims(Hk=1, Hv=2, dk=4, dv=5, K=1, conv_mode=0, act=0)
+    rng = _rng(16, C)
+    T0 = rng.normal(0, 0.5, (d.Hv, d.dk, d.dv))
+    X = rng.normal(size=(n, d.C))
+    BETA = rng.uniform(0, 1, (n, d.Hv))
+    LOGG = rng.uniform(-1, 0, (n, d.Hv))
+    parent = S.chain_tree(n)
+    q, k, v = [], [], []
+    for i in range(n):
+        qi, ki, vi = O.project(np.zeros((0, d.C)), X[i], None, d)
+        q.append(qi); k.append(ki); v.append(vi)
+    q, k, v = np.array(q), np.array(k), np.array(v)
+    res = O.verify_tree(T0, np.zeros((0, d.C)), parent, X, BETA, LOGG, None, d, [n - 1])
+    for h in range(d.Hv):
+        o, U, T_end = _chunked_chain_form(T0[h], q[:, 0], k[:, 0], v[:, h], BETA[:, h], np.exp(LOGG[:, h]), C)
+        np.testing.assert_allclose(res["o"][:, h], o, atol=1e-12)
+        np.testing.assert_allclose(res["u"][:, h], U, atol=1e-12)
+        np.testing.assert_allclose(res["boundary"][0, h], T_end, atol=1e-12)
+
+
 def test_factors_replay_the_accepted_path():
     # the factor bank (k, u, a) alone reproduces the committed state: T <- exp(a) T + k u^T
     d, rng = D_CONV, _rng(13)
