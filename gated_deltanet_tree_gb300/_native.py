@@ -100,9 +100,11 @@ def lib():
         L.gdn_commit_fold.argtypes = [P(gdn_dims), c_i32, P(gdn_batch_schedule), c_p, c_p, c_i32, P(gdn_banks), c_p]
         L.gdn_finish.argtypes = [P(gdn_dims), c_i32, c_i32, c_p, c_p, P(gdn_banks), c_p]
         L.gdn_check_error.argtypes = [P(gdn_banks), c_p]
+        L.gdn_selftest_wait_timeout.argtypes = [P(gdn_banks), c_p]
         for name in ("gdn_hld_schedule", "gdn_pack_schedules", "gdn_pack_schedules_per_node", "gdn_ddtree_build",
                      "gdn_ddtree_build_batch", "gdn_banks_init", "gdn_tree_verify",
-                     "gdn_tree_verify_noalloc", "gdn_commit_fold", "gdn_finish", "gdn_check_error"):
+                     "gdn_tree_verify_noalloc", "gdn_commit_fold", "gdn_finish", "gdn_check_error",
+                     "gdn_selftest_wait_timeout"):
             getattr(L, name).restype = c_i32
         _lib = L
     return _lib
@@ -259,3 +261,7 @@ def gdn_finish(dims: gdn_dims, B: int, layers: int, state, conv_state, banks: gd
 
 def gdn_check_error(banks: gdn_banks, stream=None):
     _check(lib().gdn_check_error(ctypes.byref(banks), _stream(stream)))
+
+
+def gdn_selftest_wait_timeout(banks: gdn_banks, stream=None):
+    _check(lib().gdn_selftest_wait_timeout(ctypes.byref(banks), _stream(stream)))

@@ -284,6 +284,30 @@ gdn_status gdn_finish(const gdn_dims* d, int32_t B, int32_t layers, float* state
   return GDN_OK;
 }
 
+namespace {
+// One CTA waits on an mbarrier armed for 16 bytes that no copy delivers: the bounded wait gives up and the
+// CTA reports the timeout like the verify kernels do.
+__global__ void selftest_wait_timeout_kernel(int32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    gdn::mbar_init(&bar);
+    gdn::mbar_expect(&bar, 16);
+  }
+  __syncthreads();
+  if (!__syncthreads_and(gdn::mbar_wait(&bar, 0)) && threadIdx.x == 0) gdn::device_error(err, GDN_DEVERR_TIMEOUT, 0);
+}
+}  // namespace
+
+gdn_status gdn_selftest_wait_timeout(gdn_banks* banks, cudaStream_t stream) {
+  gdn::clear_error();
+  if (!banks || !banks->err) return fail(GDN_ERR_INVALID_ARG, "banks / banks.err is NULL");
+  if (!aligned16(banks->err)) return fail(GDN_ERR_INVALID_ARG, "banks.err is not 16-byte aligned");
+  selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(banks->err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return GDN_OK;
+}
+
 gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream) {
   gdn::clear_error();
   if (!banks || !banks->err) return fail(GDN_ERR_INVALID_ARG, "banks / banks.err is NULL");

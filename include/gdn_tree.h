@@ -348,6 +348,22 @@ gdn_status gdn_finish(const gdn_dims* d, int32_t B, int32_t layers, float* state
  * status of the first device error (GDN_ERR_INVALID_PATH). */
 gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * gdn_selftest_wait_timeout -- exercises the give-up path of the library's
+ * bounded waits.  The source pages have no counterpart: this is a test hook.
+ *
+ * Launches one CTA on `stream` that arms an mbarrier for 16 bytes no copy
+ * will deliver and waits on it with the same bound as every wait in the
+ * verify kernels (2^28 clock cycles, ~0.13 s).  The wait gives up, the CTA
+ * sets GDN_DEVERR_TIMEOUT in banks->err (request 0) and returns; nothing
+ * faults or traps, and the context stays usable.  gdn_check_error() then
+ * reports GDN_ERR_TIMEOUT and clears the word.
+ *   banks  only banks->err is used (device, >= 2 int32, 16-byte aligned)
+ * Returns GDN_OK once launched; GDN_ERR_INVALID_ARG for a NULL or misaligned
+ * error word, GDN_ERR_CUDA if the launch fails.
+ * ------------------------------------------------------------------------- */
+gdn_status gdn_selftest_wait_timeout(gdn_banks* banks, cudaStream_t stream);
+
 /* Thread-local description of the last failed call on this thread. */
 const char* gdn_last_error(void);
 

@@ -356,6 +356,20 @@ def test_invalid_path_sets_device_error_and_commits_nothing():
     gs.ver.check_error()
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """A wait that nothing completes gives up after its bound, the host reads GDN_ERR_TIMEOUT, and the
+    context still verifies correctly afterwards (the error word cleared by the read)."""
+    from harness import GpuSession
+    import gated_deltanet_tree_gb300 as G
+    w = S.workload(2).replace(Hk=2, Hv=6, steps=2)
+    gs = GpuSession(w)
+    G._native.gdn_selftest_wait_timeout(gs.ver.banks)
+    with pytest.raises(G.GdnError) as e:
+        gs.ver.check_error()
+    assert e.value.status == G._native.GDN_ERR_TIMEOUT
+    run_parity(w)
+
+
 def test_finish_without_pending_is_a_noop_and_commit_needs_verify():
     from harness import GpuSession
     import gated_deltanet_tree_gb300 as G
