@@ -22,9 +22,11 @@
  *    host, and never trap on the device.  Host-detectable errors (bad sizes,
  *    NULL or misaligned pointers, invalid trees) return a negative status
  *    before anything is launched; gdn_last_error() then describes it.
- *  - Device-detectable errors (an accepted path that is not a root path of the
- *    verified tree) set bits in the caller's device error words
- *    (gdn_banks.err); gdn_check_error() reads and clears them.
+ *  - Device-detectable errors set bits in the caller's device error words
+ *    (gdn_banks.err): an accepted path that is not a root path of the verified
+ *    tree (GDN_DEVERR_INVALID_PATH), packed schedule words out of range
+ *    (GDN_DEVERR_SCHEDULE), an asynchronous copy or MMA that a bounded wait gave
+ *    up on (GDN_DEVERR_TIMEOUT).  gdn_check_error() reads and clears them.
  *  - Device pointers must be 16-byte aligned.
  *  - Per-node arrays are indexed [request][layer][node][...] with a node stride
  *    of n_max; nodes are numbered so that parent[i] < i (node 0 is the root).
@@ -345,7 +347,8 @@ gdn_status gdn_finish(const gdn_dims* d, int32_t B, int32_t layers, float* state
                       gdn_banks* banks, cudaStream_t stream);
 
 /* Synchronise the stream, read and clear banks->err.  Returns GDN_OK or the
- * status of the first device error (GDN_ERR_INVALID_PATH). */
+ * status of a device error: GDN_ERR_INVALID_PATH, GDN_ERR_TIMEOUT or
+ * GDN_ERR_SCHEDULE, checked in that order. */
 gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
