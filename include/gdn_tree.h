@@ -55,7 +55,7 @@ typedef enum {
   GDN_ERR_INVALID_PATH = -3,  /* (device) an accepted path is not a root path */
   GDN_ERR_UNSUPPORTED = -4,   /* a head size or mode this build has no kernel for */
   GDN_ERR_CUDA = -5,          /* a CUDA launch or copy failed */
-  GDN_ERR_TIMEOUT = -6,       /* (device) a bounded wait on an asynchronous copy gave up */
+  GDN_ERR_TIMEOUT = -6,       /* (device) a bounded wait on an asynchronous copy or MMA gave up */
   GDN_ERR_CAPACITY = -7,      /* a buffer is smaller than the call needs */
   GDN_ERR_STATE = -8,         /* calls out of order (commit without a verify) */
   GDN_ERR_SCHEDULE = -9       /* (device) packed schedule words out of range */
@@ -66,7 +66,7 @@ typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
 /* Bits of gdn_banks.err[0]. err[1] holds 1 + the first request that set a bit. */
 #define GDN_DEVERR_INVALID_PATH 1  /* an accepted path is not a root path; nothing committed */
 #define GDN_DEVERR_SCHEDULE 2      /* packed schedule words out of range; the access was skipped */
-#define GDN_DEVERR_TIMEOUT 4       /* an asynchronous copy did not complete in time; the CTA stopped */
+#define GDN_DEVERR_TIMEOUT 4       /* an asynchronous copy or MMA did not complete in time; the CTA stopped */
 
 /* Shapes and modes of one GDN layer stack. */
 typedef struct {
