@@ -27,6 +27,14 @@
  *    tree (GDN_DEVERR_INVALID_PATH), packed schedule words out of range
  *    (GDN_DEVERR_SCHEDULE), an asynchronous copy or MMA that a bounded wait gave
  *    up on (GDN_DEVERR_TIMEOUT).  gdn_check_error() reads and clears them.
+ *    GDN_DEVERR_TIMEOUT is sticky: while it is set, every conv-window, verify and
+ *    finish kernel of every later call (not only the rest of the launch that set
+ *    it) exits at once without doing work, so outputs stay unwritten and pending
+ *    factors stay unfolded.  The host-side bank lifecycle still advances
+ *    (pend_bank, verified_bank), and gdn_commit_fold still records paths.  A
+ *    caller that reads GDN_ERR_TIMEOUT from gdn_check_error() must therefore treat
+ *    the state of the calls made since the last clean check as lost (restore it
+ *    from a checkpoint: state, conv_state and the bank fields).
  *  - Device pointers must be 16-byte aligned.
  *  - Per-node arrays are indexed [request][layer][node][...] with a node stride
  *    of n_max; nodes are numbered so that parent[i] < i (node 0 is the root).
@@ -360,7 +368,10 @@ gdn_status gdn_check_error(gdn_banks* banks, cudaStream_t stream);
  * verify kernels (2^28 clock cycles, ~0.13 s).  The wait gives up, the CTA
  * sets GDN_DEVERR_TIMEOUT in banks->err (request 0) and returns; nothing
  * faults or traps, and the context stays usable.  gdn_check_error() then
- * reports GDN_ERR_TIMEOUT and clears the word.
+ * reports GDN_ERR_TIMEOUT and clears the word.  The bit is sticky (see the
+ * conventions above): until gdn_check_error() clears it, verify and finish
+ * calls on the same banks do no work, so only call this on banks whose state
+ * may be discarded, and check the error before verifying with them again.
  *   banks  only banks->err is used (device, >= 2 int32, 16-byte aligned)
  * Returns GDN_OK once launched; GDN_ERR_INVALID_ARG for a NULL or misaligned
  * error word, GDN_ERR_CUDA if the launch fails.

@@ -228,6 +228,7 @@ class Workload:
     q_scale: float = 1.0
     l2_eps: float = 1e-6
     values: str = 'qwen'    # 'tiny' (U/N recipe) | 'qwen' (sigmoid/softplus recipe)
+    edge: str = ''          # '' or a '+'-joined set of EDGE_RECIPES overwriting some of the drawn values
 
     @property
     def C(self) -> int:
@@ -321,7 +322,41 @@ def node_inputs(w: Workload, b: int, l: int, step: int):
         beta = (1.0 / (1.0 + np.exp(-zb.astype(np.float64)))).astype(np.float32)
         zg = rg.standard_normal((n, Hv), dtype=np.float32).astype(np.float64)
         log_g = (-np.logaddexp(0.0, zg)).astype(np.float32)
+    if w.edge:
+        x, beta, log_g = apply_edges(w, x, beta, log_g)
     return _to_in_dtype(w, x), _to_in_dtype(w, beta), _to_in_dtype(w, log_g)
+
+
+# Edge-case recipes: deterministic overwrites of the drawn values that drive the method into its degenerate
+# cases.  Node and head selections depend only on indices, so every (request, layer, step) block gets them.
+EDGE_RECIPES = {
+    "gate_zero": "log-gate -inf (g = 0, full forget) on every third node (1, 4, 7, ...) of the even v-heads",
+    "gate_floor": "log-gate -14 (g = 8.3e-7) on every node of v-heads h % 3 == 1, so gate products fall below "
+                  "1e-12 after two nodes",
+    "beta01": "beta = 0 on odd nodes, beta = 1 on even nodes",
+    "zero_rows": "raw input row all zeros on nodes 2, 5, 8, ... (with the conv: also k-head 0's conv taps zero)",
+}
+
+
+def apply_edges(w: Workload, x: np.ndarray, beta: np.ndarray, log_g: np.ndarray):
+    """x [n, C], beta/log_g [n, Hv] float32 -> copies with the workload's edge recipes applied."""
+    x, beta, log_g = x.copy(), beta.copy(), log_g.copy()
+    n = x.shape[0]
+    nodes = np.arange(n)
+    heads = np.arange(w.Hv)
+    for e in w.edge.split("+"):
+        if e == "gate_zero":
+            log_g[np.ix_(nodes % 3 == 1, heads % 2 == 0)] = -np.inf
+        elif e == "gate_floor":
+            log_g[:, heads % 3 == 1] = -14.0
+        elif e == "beta01":
+            beta[nodes % 2 == 1] = 0.0
+            beta[nodes % 2 == 0] = 1.0
+        elif e == "zero_rows":
+            x[nodes % 3 == 2] = 0.0
+        else:
+            raise ValueError(f"unknown edge recipe {e!r}")
+    return x, beta, log_g
 
 
 def init_state(w: Workload, b: int, l: int) -> np.ndarray:
@@ -339,7 +374,10 @@ def init_conv_state(w: Workload, b: int, l: int) -> np.ndarray:
 def conv_weight(w: Workload, l: int) -> np.ndarray:
     """Depthwise conv weights of one layer: [C, K] fp32, N(0, 1/K)."""
     r = rng_for(w.cfg, S_CONVW, l)
-    return (r.standard_normal((w.C, w.K), dtype=np.float32) * np.float32(1.0 / np.sqrt(w.K))).astype(np.float32)
+    cw = (r.standard_normal((w.C, w.K), dtype=np.float32) * np.float32(1.0 / np.sqrt(w.K))).astype(np.float32)
+    if "zero_rows" in w.edge.split("+"):   # k-head 0 convolves to zero: only eps keeps its k_hat finite
+        cw[w.Hk * w.dk:w.Hk * w.dk + w.dk] = 0.0
+    return cw
 
 
 def step_trees(w: Workload, step: int) -> List[np.ndarray]:

@@ -240,6 +240,26 @@ def test_ddtree64_top8_single_layer(kernel):
     run_parity(w, kernel=kernel)
 
 
+# the method's degenerate cases, driven through every verify kernel: each variant below changes the Qwen-like
+# layer (128-wide heads, 22-node DDTrees, fold of the previous step's path) in one way
+EDGE_VARIANTS = {
+    "gate_zero": dict(edge="gate_zero"),                        # log g = -inf: g = 0, the state is forgotten
+    "gate_floor": dict(edge="gate_floor", path_max=22),         # gate products below 1e-12 (the lazy decay's floor)
+    "beta01": dict(edge="beta01"),                              # beta = 0 writes nothing; beta = 1 with |k| = 1
+    "zero_rows_bypass": dict(edge="zero_rows", conv_mode=0, act=0),   # q = k = 0: eps alone keeps q_hat, k_hat finite
+    "zero_rows_conv": dict(edge="zero_rows"),                   # k-head 0 convolves to zero
+    "q_scale": dict(q_scale=float(1.0 / np.sqrt(128.0))),       # the Qwen-style query scale
+    "fp32_inputs": dict(in_dtype=S.DTYPE_F32),                  # fp32 x, beta, log g at 128-wide heads
+}
+
+
+@pytest.mark.parametrize("variant", sorted(EDGE_VARIANTS))
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_edge_cases(variant, kernel):
+    w = S.workload(2).replace(Hk=2, Hv=6, B=2, layers=2, steps=3, **EDGE_VARIANTS[variant])
+    run_parity(w, kernel=kernel)
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled units
 # ---------------------------------------------------------------------------
@@ -368,6 +388,31 @@ def test_bounded_wait_gives_up_and_reports_timeout():
         gs.ver.check_error()
     assert e.value.status == G._native.GDN_ERR_TIMEOUT
     run_parity(w)
+
+
+def test_timeout_bit_is_sticky_until_checked():
+    """While GDN_DEVERR_TIMEOUT is set, later verify and finish calls on the same banks do no work (outputs
+    and state untouched) until gdn_check_error reads and clears it; afterwards the banks verify normally."""
+    from harness import GpuSession
+    import gated_deltanet_tree_gb300 as G
+    w = S.workload(2).replace(Hk=2, Hv=6, steps=2)
+    gs = GpuSession(w)
+    gs.verify(0)
+    gs.commit(0)
+    torch.cuda.synchronize()
+    gs.ver.check_error()
+    G._native.gdn_selftest_wait_timeout(gs.ver.banks)
+    state0, o0 = gs.state.clone(), gs.out_o.clone()
+    gs.out_o.fill_(7.0)
+    gs.verify(1)                        # no check in between: the pending fold and the verify must not run
+    torch.cuda.synchronize()
+    assert torch.equal(gs.state, state0)
+    assert bool((gs.out_o == 7.0).all())
+    with pytest.raises(G.GdnError) as e:
+        gs.ver.check_error()
+    assert e.value.status == G._native.GDN_ERR_TIMEOUT
+    gs.ver.check_error()                # cleared by the read
+    run_parity(w)                       # a fresh session on the same context is unaffected
 
 
 def test_finish_without_pending_is_a_noop_and_commit_needs_verify():

@@ -180,6 +180,87 @@ def test_head_split_and_gqa_map():
     assert np.all(T[3:] == 0)
 
 
+def test_bf16_decode_against_torch_and_by_hand():
+    """as_f64 on bf16 bit patterns equals torch's bfloat16 -> float64 conversion on random patterns and on
+    the special values (+-0, subnormals, the extreme normals, +-inf); a few patterns are decoded by hand from
+    the format (1 sign, 8 exponent bits with bias 127, 7 fraction bits)."""
+    import torch
+    rng = _rng(30)
+    bits = rng.integers(0, 1 << 16, 20000, dtype=np.uint32).astype(np.uint16)
+    special = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80,
+                        0x3F80, 0xC000, 0x3E80, 0x4049], dtype=np.uint16)
+    allbits = np.concatenate([bits, special])
+    finite = (allbits & 0x7F80) != 0x7F80
+    finite |= (allbits & 0x7F) == 0            # keep +-inf, drop NaN patterns (NaN != NaN)
+    allbits = allbits[finite]
+    ref = torch.from_numpy(allbits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = O.as_f64(allbits, O.DTYPE_BF16)
+    np.testing.assert_array_equal(got, ref)
+    assert np.signbit(O.as_f64(np.array([0x8000], np.uint16), O.DTYPE_BF16)[0])
+    hand = {0x3F80: 1.0, 0xC000: -2.0, 0x3E80: 0.25, 0x4049: 3.140625, 0x0001: 2.0 ** -133,
+            0x0080: 2.0 ** -126, 0x7F7F: (2.0 - 2.0 ** -7) * 2.0 ** 127, 0xFF80: -np.inf}
+    for b, v in hand.items():
+        assert O.as_f64(np.array([b], np.uint16), O.DTYPE_BF16)[0] == v, hex(b)
+    # fp32 inputs are upcast unchanged
+    x = rng.normal(size=100).astype(np.float32)
+    np.testing.assert_array_equal(O.as_f64(x, O.DTYPE_F32), x.astype(np.float64))
+
+
+@pytest.mark.parametrize("conv_mode", [0, 1])
+def test_q_scale_multiplies_the_output_only(conv_mode):
+    """The printed rule gives o = S' q_hat; a query scale s multiplies the normalised q, so o(s) = s o(1)
+    while u, k_hat and every state are unchanged.  A scale applied before the L2 normalisation would cancel
+    (o(s) = o(1)) and fails this."""
+    import dataclasses
+    d1 = O.Dims(Hk=2, Hv=4, dk=4, dv=6, K=4, conv_mode=conv_mode, act=1)
+    rng = _rng(31)
+    parent = np.array([-1, 0, 1, 1, 0, 4], dtype=np.int32)
+    T, W, X, BETA, LOGG, cw = _rand_inputs(d1, len(parent), rng)
+    base = O.verify_tree(T, W, parent, X, BETA, LOGG, cw, d1)
+    for s in (0.5, 1.0 / np.sqrt(d1.dk), 3.0):
+        ds = dataclasses.replace(d1, q_scale=s)
+        r = O.verify_tree(T, W, parent, X, BETA, LOGG, cw, ds)
+        np.testing.assert_allclose(r["o"], s * base["o"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(r["u"], base["u"], rtol=0, atol=0)
+        np.testing.assert_allclose(r["k"], base["k"], rtol=0, atol=0)
+        np.testing.assert_allclose(r["boundary"], base["boundary"], rtol=0, atol=0)
+        assert not np.allclose(r["o"], base["o"])
+    # one token by hand: with T = 0, beta = 1, g = 1: T' = k v^T, so o = s (k_hat . q_hat) v
+    d = O.Dims(Hk=1, Hv=1, dk=2, dv=2, K=1, conv_mode=0, act=0, l2_eps=0.0, q_scale=0.25)
+    x = np.array([3.0, 4.0, 1.0, 0.0, 2.0, -1.0])          # q = (3, 4), k = (1, 0), v = (2, -1)
+    _, _, o, _, _ = O.token_step(np.zeros((1, 2, 2)), np.zeros((0, 6)), x, np.ones(1), np.zeros(1), None, d)
+    np.testing.assert_allclose(o[0], 0.25 * (3.0 / 5.0) * np.array([2.0, -1.0]), atol=1e-15)
+
+
+def test_edge_recipes_reach_the_degenerate_cases():
+    """The seeded edge-case inputs the GPU parity tests use do what they are named for, and the oracle's
+    results on them keep the closed forms: g = 0 forgets the state, beta = 0 writes nothing, an all-zero
+    row (bypass mode) has q_hat = k_hat = 0 so its o is 0 and its u is beta v."""
+    w = S.workload(1).replace(Hk=2, Hv=6, conv_mode=0, act=0, edge="gate_zero+beta01+zero_rows", budget=8)
+    x, be, ag = (O.as_f64(a, w.in_dtype) for a in S.node_inputs(w, 0, 0, 0))
+    assert np.isneginf(ag[1, 0]) and np.isfinite(ag[1, 1]) and np.isneginf(ag[4, 2])
+    assert np.all(be[1::2] == 0) and np.all(be[0::2] == 1) and np.all(x[2::3] == 0)
+    d = O.dims_of(w)
+    parent = np.arange(-1, 7, dtype=np.int32)              # a chain
+    T0 = S.init_state(w, 0, 0).astype(np.float64)
+    r = O.verify_tree(T0, np.zeros((w.K - 1, w.C)), parent, x, be, ag, None, d)
+    assert np.all(np.isfinite(r["o"])) and np.all(np.isfinite(r["u"]))
+    np.testing.assert_array_equal(r["o"][2], 0.0)          # zero row: q_hat = 0
+    np.testing.assert_allclose(r["u"][2], be[2][:, None] * x[2, 2 * w.Hk * w.dk:].reshape(w.Hv, w.dv), atol=0)
+    np.testing.assert_array_equal(r["u"][1], 0.0)          # beta = 0 on node 1
+    # node 1 forgets the even heads' state: the state after node 1 is beta k v^T = 0 there (beta = 0)
+    Tn, Wn = T0.copy(), np.zeros((w.K - 1, w.C))
+    for m in (0, 1):
+        Tn, Wn, _, _, _ = O.token_step(Tn, Wn, x[m], be[m], ag[m], None, d)
+    np.testing.assert_array_equal(Tn[0::2], 0.0)
+    wf = S.workload(1).replace(edge="gate_floor", Hk=2, Hv=6)
+    _, _, agf = S.node_inputs(wf, 0, 0, 0)
+    assert np.all(agf[:, 1::3] == -14.0) and np.exp(-28.0) < 1e-12
+    wz = S.workload(1).replace(edge="zero_rows", Hk=2, Hv=6)
+    cwz = S.conv_weight(wz, 0)
+    assert np.all(cwz[wz.Hk * wz.dk:wz.Hk * wz.dk + wz.dk] == 0) and np.any(cwz[wz.Hk * wz.dk + wz.dk:] != 0)
+
+
 # ---------------------------------------------------------------------------
 # tree semantics
 # ---------------------------------------------------------------------------

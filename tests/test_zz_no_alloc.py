@@ -4,8 +4,8 @@ Callers running inside a stream capture, engines whose device pool belongs to
 their own allocator, and plugins handed only buffers and a stream cannot pass
 the workspace gdn_tree_verify asks for.  The no-allocation entry point uses the
 library's fixed device scratch instead.  These tests call it through the C ABI
-and check that two calls in a row give what the workspace entry point gives on
-the same inputs, and that a batch too large for the fixed scratch is refused
+and check that two calls in a row give, bit for bit, what the workspace entry
+point gives on the same inputs, and that a batch too large for the fixed scratch is refused
 before anything runs.  This file is collected last on purpose.
 """
 import numpy as np
@@ -13,7 +13,6 @@ import pytest
 import torch
 
 import synthetic as S
-from parity import O_TOL, STATE_TOL, U_TOL, K_TOL
 
 pytestmark = pytest.mark.gpu
 
@@ -24,16 +23,9 @@ def built():
     build()
 
 
-def _max_rel(a, b):
-    return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
-
-
-def _head_frob(a, b):
-    d = (a - b).flatten(-2).norm(dim=-1)
-    return float((d / b.flatten(-2).norm(dim=-1).clamp_min(1e-30)).max())
-
-
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
+    # both entry points launch the same kernels on the same inputs, so every result must be bit-identical
+    # (which is within every tolerance the parity tests use); a difference would point at scratch addressing
     from gated_deltanet_tree_gb300 import _native as N
     from harness import GpuSession, WorkloadPlan
     w = S.workload(2).replace(steps=2)
@@ -48,13 +40,14 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         torch.cuda.synchronize()
         n = len(plan.trees[s][0])
         nb = new.schedule(s).nb_max
-        assert _max_rel(new.out_o[0, 0, :n], ref.out_o[0, 0, :n]) <= O_TOL
-        assert _head_frob(new.state, ref.state) <= STATE_TOL
-        assert _head_frob(new.boundary[:, :, :nb], ref.boundary[:, :, :nb]) <= STATE_TOL
+        assert torch.equal(new.out_o[:, :, :n], ref.out_o[:, :, :n])
+        assert torch.equal(new.state, ref.state)
+        assert torch.equal(new.conv_state, ref.conv_state)
+        assert torch.equal(new.boundary[:, :, :nb], ref.boundary[:, :, :nb])
         bank = new.ver.banks.verified_bank
         assert bank == ref.ver.banks.verified_bank
-        assert float((new.ver.bank_view("k", bank) - ref.ver.bank_view("k", bank)).abs().max()) <= K_TOL
-        assert _max_rel(new.ver.bank_view("u", bank), ref.ver.bank_view("u", bank)) <= U_TOL
+        for f in ("k", "u", "a", "x"):
+            assert torch.equal(new.ver.bank_view(f, bank)[:, :, :n], ref.ver.bank_view(f, bank)[:, :, :n]), f
         ref.commit(s)
         new.commit(s)
     new.ver.check_error()
