@@ -436,9 +436,10 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
 
     # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
     # A/B: the same steps with per-node-state schedules (every node reloads its parent's stored state)
-    ab = walk = simt = None
+    ab = walk = simt = tc1 = None
     if not args.no_ab:
         if tc_applies(w) and not any(walks[args.warmup:]):
+            tc1 = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="tc_per_head")
             simt = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="ut_simt")
         walk = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="walk")
         ab = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="per_node")
@@ -460,7 +461,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
                                 (clk or {}).get("sm_max_mhz") or 2070.0)
     return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab, walk=walk,
-                simt=simt, avg_tflops=avg_tflops,
+                simt=simt, tc1=tc1, avg_tflops=avg_tflops,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap, walked=any(walks[args.warmup:]),
@@ -483,7 +484,8 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode):
         packed.append(torch.from_numpy(words).to(dev))
         nb_cap = max(nb_cap, nb)
         depth.append(dm)
-    flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | (N.GDN_VERIFY_UT_SIMT if mode == "ut_simt" else N.GDN_VERIFY_CHAIN_WALK)
+    flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | {"ut_simt": N.GDN_VERIFY_UT_SIMT, "tc_per_head": N.GDN_VERIFY_TC_PER_HEAD}.get(
+        mode, N.GDN_VERIFY_CHAIN_WALK)
     boundary = torch.empty(w.B, w.layers, nb_cap, w.Hv, w.dk, w.dv, dtype=torch.float32, device=dev)
     ver = gs.ver
 
@@ -512,7 +514,8 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode):
     torch.cuda.empty_cache()
     return {"schedule": {"per_node": "per-node states in HBM (no heavy edges)",
                          "walk": "heavy-light chain walk, branch states in tensor memory",
-                         "ut_simt": "tree-masked UT form on the CUDA cores (ut_verify_kernel)"}[mode],
+                         "ut_simt": "tree-masked UT form on the CUDA cores (ut_verify_kernel)",
+                         "tc_per_head": "tree-masked UT form on the tensor cores, a CTA per v-head (ut_tc_verify_kernel)"}[mode],
             "steps": steps, "nb_max": nb_cap,
             "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
@@ -671,7 +674,7 @@ def main():
                      else "alu",
                      "kernel": "gdn_tree_verify (conv_window_kernel + "
                                + ("chain_verify_kernel)" if r["walked"] else
-                                  "ut_tc_verify_kernel)" if tc_applies(w) else "ut_verify_kernel)"),
+                                  "ut_tcp_verify_kernel)" if tc_applies(w) else "ut_verify_kernel)"),
                      "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
@@ -694,6 +697,8 @@ def main():
             "host_per_step": ("DDTree construction from the draft tables, " if w.tree == "ddtree" else "")
                              + "heavy-light schedules, packing"},
         "gpu_launches": r["gpu_launches"],
+        "ab_tc_per_head": None if r["tc1"] is None else dict(
+            r["tc1"], persistent_speedup=r["tc1"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_ut_simt": None if r["simt"] is None else dict(
             r["simt"], tc_speedup=r["simt"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_chain_walk": None if r["walk"] is None else dict(

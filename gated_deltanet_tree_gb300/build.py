@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgdn_tree.so")
 
-SOURCES = ["hld_schedule.cpp", "ddtree.cpp", "gdn_abi.cu", "gdn_conv.cu", "gdn_verify.cu", "gdn_verify_ut.cu", "gdn_verify_tc.cu", "gdn_commit.cu", "gdn_noalloc.cu"]
+SOURCES = ["hld_schedule.cpp", "ddtree.cpp", "gdn_abi.cu", "gdn_conv.cu", "gdn_verify.cu", "gdn_verify_ut.cu", "gdn_verify_tc.cu", "gdn_verify_tcp.cu", "gdn_commit.cu", "gdn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -149,7 +149,7 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
                            float* conv_state, float* out_o, float* boundary_states, gdn_banks* banks,
                            void* workspace, size_t workspace_bytes, int32_t flags, cudaStream_t stream) {
   gdn::clear_error();
-  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT))
+  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD))
     return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
   GDN_TRY(check_dims(d));
   GDN_TRY(check_sched(sched));
@@ -208,6 +208,10 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   if (vp.chain_walk) {
     e = gdn::launch_verify(vp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "chain-verify launch");
+  } else if (!(flags & (GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD)) &&
+             gdn::verify_tcp_supported(d->dk, d->dv, n_max)) {
+    e = gdn::launch_verify_tcp(vp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, persistent)");
   } else if (!(flags & GDN_VERIFY_UT_SIMT) && gdn::verify_tc_supported(d->dk, d->dv, n_max)) {
     e = gdn::launch_verify_tc(vp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores)");

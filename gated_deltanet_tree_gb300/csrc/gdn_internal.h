@@ -150,8 +150,10 @@ struct CommitParams {
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);      // chain walk; also the fold-only launches
 cudaError_t launch_verify_ut(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, CUDA cores
-cudaError_t launch_verify_tc(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, tensor cores
+cudaError_t launch_verify_tc(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, tensor cores, a CTA per head
 bool verify_tc_supported(int dk, int dv, int n_max);
+cudaError_t launch_verify_tcp(const VerifyParams& p, cudaStream_t s);  // the same, persistent and warp-specialised
+bool verify_tcp_supported(int dk, int dv, int n_max);
 
 cudaError_t launch_commit(const CommitParams& p, int compact, cudaStream_t s);
 bool verify_supported(int dk, int dv);

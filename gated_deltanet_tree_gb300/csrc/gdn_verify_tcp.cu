@@ -1,0 +1,739 @@
+// Tree verify in the tree-masked UT form on the tensor cores, persistent and
+// warp-specialised.
+//
+// SpecLA article, "状态驻留验证" (the topology-masked UT decomposition; one state
+// read and one committed write per head) and "延迟融合提交" (the pending path
+// folded into the state tile at load).  With T0 the committed state after the
+// fold, Gamma_t the product of the gates on the root path up to node t,
+// rho_ts = Gamma_t / Gamma_s, G_ts = k_t . k_s and H_ts = q_t . k_s:
+//   u_t = beta_t v_t - beta_t Gamma_t (T0^T k_t) - sum_{s ancestor of t} beta_t rho_ts G_ts u_s
+//   o_t = Gamma_t (T0^T q_t) + H_tt u_t + sum_{s ancestor of t} rho_ts H_ts u_s.
+// T0^T [k_0 .. k_{n-1} q_0 .. q_{n-1}] is the dense part (tcgen05 MMAs of kind
+// tf32, split three ways for fp32 accuracy); the rest is per d_v column.
+//
+// Launch: one CTA per SM, looping over work items.  An item is one (request,
+// layer, k-head) with its R v-heads (or a single v-head when the batch is too
+// small to fill the SMs).  Roles:
+//   - NG compute groups of 128 threads (one warpgroup each).  Thread c of a group
+//     owns d_v column c of the state, which is also its tensor-memory lane.  The
+//     groups take the CTA's items in turn, so one group's fold, tables and
+//     epilogue run while the other's MMAs and loads are in flight.  The first
+//     thread of a group issues the group's tcgen05.mma (no separate MMA warp: with
+//     eight warps, two per SM sub-partition, a thread may hold the whole state
+//     column in registers).
+// Per item a group builds the [k | q] operand (tf32 high and low parts) and the
+// Gram coefficients of every ancestor pair on the CUDA cores, from the k and q
+// rows a TMA copy brought in while the previous item ran.  Per v-head:
+//   1. fold the pending path into the state column held in registers (the
+//      column was loaded while the previous head finished) and write T0 once;
+//   2. T0^T (tf32 high part) into the group's tensor-memory A columns, times all
+//      4 NB operand rows into the D columns; then the low part of T0^T times the
+//      high rows, accumulated;
+//   3. meanwhile rho, Gamma and the pair coefficients of this head's gates;
+//   4. once the A columns are read, the next head's state column is loaded into
+//      the registers;
+//   5. epilogue: per column c, a forward substitution over the nodes in order,
+//      u_t = B_t - sum A_ts u_s, o_t = Gamma_t (T0^T q_t) + H_tt u_t + sum C_ts u_s,
+//      with T0^T k_t and T0^T q_t read from tensor memory and u_s from shared
+//      memory; u and o are stored as they are formed.
+// The v rows, the pending rows and the next item's k and q rows arrive by TMA
+// bulk copies issued one head (or one item) ahead, and the state tiles two heads
+// ahead are prefetched into L2, so the loads of later heads are in flight while
+// the current one computes.
+//
+// Tensor memory per group g (256 columns): [256 g, +d_k) A = T0^T, first its high
+// then its low part; [256 g + 128, +4 NB) D, with T0^T k_t = D[t] + D[2 NB + t]
+// and T0^T q_t = D[NB + t] + D[3 NB + t] (NB = n rounded up to 8).
+//
+// Every wait is bounded.  A wait that gives up flags GDN_DEVERR_TIMEOUT and sets
+// the CTA's abort word; every role then stops at its next wait, waits (bounded)
+// for the copies and MMAs it has in flight, and the CTA frees its tensor memory
+// and exits.
+#include "gdn_tile.cuh"
+#include "gdn_umma.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kPDv = 128;          // d_v: the MMA's M and the threads of a group
+constexpr int kPGroup = 128;       // threads per compute group
+constexpr int kPFold = 8;          // pending rows staged per fold chunk
+constexpr int kPMaxNodes = 32;     // 4 NB <= 128 D columns
+
+// ---- small PTX helpers
+// One non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Bounded wait that also gives up once the CTA's abort word is set.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, const volatile int* abortw) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    if (*abortw) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+// Barrier of one compute group (named barrier id, 128 threads); the AND of `v` over the group.
+__device__ __forceinline__ bool group_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(kPGroup)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kPGroup) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t ta, float (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "r"(ta)
+               : "memory");
+}
+
+// ColTile::advance (one node of the gated delta rule on the lazily decayed column) with the same operands
+// in the same order, so the results are bit-identical; the k row is read 16 values at a time, with a
+// compiler barrier between the pieces, so a whole 128-row column plus its k row never need registers at once.
+template <int NR>
+__device__ __forceinline__ float fold_node(ColTile<NR>& R, const float* krows, float gam1, float u) {
+  if (gam1 < kGammaFloor) {
+    R.materialise(gam1);
+    gam1 = 1.f;
+  }
+  const float r = __fdividef(1.f, gam1);
+  const float ut = u * r;
+  const u64 u2 = pack2(ut, ut);
+  const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(krows);
+#pragma unroll
+  for (int j4 = 0; j4 < NR / 4; ++j4) {
+    const ulonglong2 kk = k4[j4];
+    R.T[2 * j4 + 0] = fma2(kk.x, u2, R.T[2 * j4 + 0]);
+    R.T[2 * j4 + 1] = fma2(kk.y, u2, R.T[2 * j4 + 1]);
+    if ((j4 & 3) == 3) asm volatile("" ::: "memory");
+  }
+  return gam1;
+}
+
+// Shared-memory layout in bytes: NG group regions, then the CTA's barriers and words.
+struct PLayout {
+  int n_max, dk;
+  __host__ __device__ static int a16(int x) { return (x + 15) & ~15; }
+  __host__ __device__ int nbm() const { return (n_max + 7) & ~7; }
+  __host__ __device__ int pairs() const { return n_max * (n_max - 1) / 2; }
+  __host__ __device__ int words() const { return 5 + 4 * n_max; }
+  // one group's region
+  __host__ __device__ int opnd() const { return 0; }                                 // [dk/4][4 NB][16 B] operand
+  __host__ __device__ int stg() const { return opnd() + 4 * nbm() * dk * 4; }         // [2][n_max][dk] k, q rows
+  __host__ __device__ int vbuf() const { return stg() + 2 * n_max * dk * 4; }         // [n_max][128] v, then u
+  __host__ __device__ int pk() const { return vbuf() + n_max * kPDv * 4; }            // [kPFold][dk] pending k
+  __host__ __device__ int pu() const { return pk() + kPFold * dk * 4; }               // [kPFold][128] pending u
+  __host__ __device__ int ptab() const { return pu() + kPFold * kPDv * 4; }           // [pairs] (A, C, s dv, -)
+  __host__ __device__ int hsc() const { return ptab() + a16(pairs() * 16); }          // [n_max] (g, beta, bG, G)
+  __host__ __device__ int gh() const { return hsc() + n_max * 16; }                   // [pairs] (G_ts, H_ts)
+  __host__ __device__ int hd() const { return gh() + a16(pairs() * 8); }              // [n_max] H_tt
+  __host__ __device__ int pgt() const { return hd() + a16(n_max * 4); }               // [n_max] pending gates
+  __host__ __device__ int rec() const { return pgt() + a16(n_max * 4); }              // [words] schedule record
+  __host__ __device__ int path() const { return rec() + a16(words() * 4); }           // [n_max] pending path
+  __host__ __device__ int dep() const { return path() + a16(n_max * 4); }             // [n_max] depth
+  __host__ __device__ int coff() const { return dep() + a16(n_max * 4); }             // [n_max + 1] pair offsets
+  __host__ __device__ int ranc() const { return coff() + a16((n_max + 1) * 4); }      // [pairs] ancestor
+  __host__ __device__ int ptn() const { return ranc() + a16(pairs() * 4); }           // [pairs] node
+  __host__ __device__ int group_bytes() const { return (ptn() + a16(pairs() * 4) + 127) & ~127; }
+  // CTA words: [ng][4] mbarriers (k/q rows, v rows, pending rows, MMA done), the tensor-memory base and
+  // the abort word
+  __host__ __device__ int shared(int ng) const { return ng * group_bytes(); }
+  __host__ __device__ int bytes(int ng) const { return shared(ng) + ng * 4 * 8 + 16; }
+};
+
+template <int DK, typename InT, int NG>
+__global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyParams p, int n_items, int hpi) {
+  constexpr int DV = kPDv;
+  constexpr int KC = DK / 4;                    // 16-byte chunks of a k or q row
+  constexpr unsigned FULL = 0xffffffffu;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const PLayout L{p.n_max, DK};
+  const int n_max = p.n_max;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = warp >> 2;                      // compute group
+  unsigned char* shr = smem + L.shared(NG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(shr);                  // [NG][4]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + NG * 4);
+  volatile int* abortw = reinterpret_cast<volatile int*>(tslot + 1);
+
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tslot, NG * 256);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int i = 0; i < NG * 4; ++i) mbar_init(bars + i);
+    *abortw = launch_aborted(p.err) ? 1 : 0;   // an earlier launch or CTA gave up on a wait
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tbase = *tslot;
+  const int ipb = p.Hv / hpi;                   // items per (request, layer)
+  const InT* beta = static_cast<const InT*>(p.beta);
+  const InT* logg = static_cast<const InT*>(p.log_g);
+  const SchedLayout lay{n_max};
+
+  {
+    // ============================ compute group ============================
+    const int c = tid - g * kPGroup;            // d_v column = tensor-memory lane
+    const int wq = c >> 5;                      // warp within the group = lane quarter
+    const int gid = 1 + g;                      // named barrier of the group
+    unsigned char* gb = smem + g * L.group_bytes();
+    float* opnd = reinterpret_cast<float*>(gb + L.opnd());
+    float* stg = reinterpret_cast<float*>(gb + L.stg());
+    float* vbuf = reinterpret_cast<float*>(gb + L.vbuf());
+    float* pk = reinterpret_cast<float*>(gb + L.pk());
+    float* pu = reinterpret_cast<float*>(gb + L.pu());
+    float4* ptab = reinterpret_cast<float4*>(gb + L.ptab());
+    float4* hsc = reinterpret_cast<float4*>(gb + L.hsc());
+    float2* gh = reinterpret_cast<float2*>(gb + L.gh());
+    float* hd = reinterpret_cast<float*>(gb + L.hd());
+    float* pgt = reinterpret_cast<float*>(gb + L.pgt());
+    int32_t* rec = reinterpret_cast<int32_t*>(gb + L.rec());
+    int32_t* spath = reinterpret_cast<int32_t*>(gb + L.path());
+    int32_t* dep = reinterpret_cast<int32_t*>(gb + L.dep());
+    int32_t* coff = reinterpret_cast<int32_t*>(gb + L.coff());
+    int32_t* ranc = reinterpret_cast<int32_t*>(gb + L.ranc());
+    int32_t* ptn = reinterpret_cast<int32_t*>(gb + L.ptn());
+    uint64_t* b_kq = bars + g * 4 + 0;
+    uint64_t* b_rows = bars + g * 4 + 1;
+    uint64_t* b_pend = bars + g * 4 + 2;
+    uint64_t* b_mma = bars + g * 4 + 3;
+    const uint32_t tA = tbase + (static_cast<uint32_t>(32 * wq) << 16) + 256u * g;   // this lane, A columns
+    const uint32_t tD = tA + 128u;                                                   // this lane, D columns
+    const int32_t* parent = rec + lay.parent();
+    const int32_t* nflags = rec + lay.nflags();
+    const int32_t* bslot = rec + lay.bslot();
+    uint32_t ph_kq = 0, ph_rows = 0, ph_pend = 0, ph_mma = 0;
+    bool armed_kq = false, armed_rows = false, armed_pend = false, armed_mma = false;
+    bool ok = true;   // group-uniform: false once a wait gave up
+
+    // ---- per-item identity
+    struct Item {
+      int it, bl, b, h0, kh;
+    };
+    auto item_at = [&](int k) {
+      Item x;
+      x.it = blockIdx.x + k * static_cast<int>(gridDim.x);
+      const int it = x.it < n_items ? x.it : 0;
+      x.bl = it / ipb;
+      x.h0 = (it % ipb) * hpi;
+      x.b = x.bl / p.layers;
+      x.kh = x.h0 / p.R;
+      return x;
+    };
+    // ---- TMA issue, warp 0 of the group (all lanes call; lane 0 arms the barrier)
+    auto issue_kq = [&](const Item& x) {   // k and q rows of all n_max node slots of the item's k-head
+      if (wq == 0) {
+        if (lane == 0) mbar_expect(b_kq, static_cast<uint32_t>(2 * n_max * DK * 4));
+        __syncwarp();
+        for (int node = lane; node < n_max; node += 32) {
+          const size_t row = static_cast<size_t>(x.bl) * n_max + node;
+          bulk_g2s(stg + node * DK, p.k_in + (row * p.Hk + x.kh) * DK, DK * 4, b_kq);
+          bulk_g2s(stg + (n_max + node) * DK, p.q_in + (row * p.Hk + x.kh) * DK, DK * 4, b_kq);
+        }
+      }
+      armed_kq = true;
+    };
+    auto issue_rows = [&](const Item& x, int h) {   // v rows of all n_max node slots of v-head h
+      if (wq == 0) {
+        if (lane == 0) mbar_expect(b_rows, static_cast<uint32_t>(n_max * DV * 4));
+        __syncwarp();
+        for (int node = lane; node < n_max; node += 32)
+          bulk_g2s(vbuf + node * DV, p.v_in + ((static_cast<size_t>(x.bl) * n_max + node) * p.Hv + h) * DV, DV * 4,
+                   b_rows);
+      }
+      armed_rows = true;
+    };
+    // pending rows f0 .. f0 + fn of v-head h; `pe` is this lane's path entry f0 + lane (warp 0)
+    auto issue_pend = [&](const Item& x, int h, int fn, int pe) {
+      if (fn <= 0) return;
+      if (wq == 0) {
+        if (lane == 0) mbar_expect(b_pend, static_cast<uint32_t>(fn * (DK + DV) * 4));
+        __syncwarp();
+        if (lane < fn) {
+          const size_t row = static_cast<size_t>(x.bl) * n_max + (pe & kPathNodeMask);
+          bulk_g2s(pk + lane * DK, p.pend_k + (row * p.Hk + x.kh) * DK, DK * 4, b_pend);
+          bulk_g2s(pu + lane * DV, p.pend_u + (row * p.Hv + h) * DV, DV * 4, b_pend);
+        }
+      }
+      armed_pend = true;
+    };
+    auto prefetch_state_l2 = [&](const Item& x, int h) {
+      if (c < 4)
+        prefetch_l2(p.state + ((static_cast<size_t>(x.bl) * p.Hv + h) * DK + c * (DK / 4)) * DV, DK / 4 * DV * 4);
+    };
+    // the state tile of the head m places after head j of item k in this group's sequence, into L2
+    auto prefetch_ahead = [&](int kk, int j, int m) {
+      const Item x = item_at(kk + NG * ((j + m) / hpi));
+      if (x.it < n_items) prefetch_state_l2(x, x.h0 + (j + m) % hpi);
+    };
+    // ---- per-item words held in registers until the item starts: schedule record, pending path entry c,
+    // pending length (-1: out of range)
+    int rw0 = 0, rw1 = 0, pth_nx = 0, lp_nx = 0;
+    auto load_item_regs = [&](const Item& x) {
+      const int32_t* r = p.words + static_cast<size_t>(x.b) * lay.words();
+      rw0 = c < lay.words() ? r[c] : 0;
+      rw1 = c + kPGroup < lay.words() ? r[c + kPGroup] : 0;
+      int lp = p.fold ? p.pend_len[x.b] : 0;
+      pth_nx = (p.fold && c < n_max) ? p.pend_path[static_cast<size_t>(x.b) * n_max + c] : 0;
+      // an entry past n_max would address outside the banks: the whole path is refused
+      const bool bad = lp < 0 || lp > n_max || (c < lp && (pth_nx & kPathNodeMask) >= n_max);
+      if (!group_and(gid, !bad)) lp = -1;
+      lp_nx = lp;
+    };
+    // ---- per-head values held in registers until the head starts: node c's log-gate and beta, the gate
+    // of pending node c
+    float ra = 0.f, rb = 0.f, rpg = 1.f;
+    auto load_head_regs = [&](const Item& x, int h, int lp, int pe) {
+      const size_t row = static_cast<size_t>(x.bl) * n_max + c;
+      if (c < n_max) {
+        ra = load_in<InT>(logg, row * p.Hv + h);
+        rb = load_in<InT>(beta, row * p.Hv + h);
+      }
+      if (c < lp) rpg = expf(p.pend_a[(static_cast<size_t>(x.bl) * n_max + (pe & kPathNodeMask)) * p.Hv + h]);
+    };
+    // ---- the group's MMAs (thread c == 0): high pass A_hi x [k_hi | q_hi | k_lo | q_lo] (N = 4 NB) into D,
+    // or low pass A_lo x [k_hi | q_hi] (N = 2 NB) accumulated; completion arrives on b_mma
+    auto issue_mma = [&](bool hi, int NB) {
+      const uint32_t a = tbase + 256u * g, d = a + 128u;
+      const uint32_t lbo = static_cast<uint32_t>(4 * NB) * 16u;   // K-adjacent core matrices
+      const uint64_t d0 = umma_desc(smem_addr(opnd), lbo, 128u), step = static_cast<uint64_t>((2u * lbo) >> 4);
+      const uint32_t id = umma_idesc_tf32(128, hi ? 4 * NB : 2 * NB);
+#pragma unroll
+      for (int s = 0; s < DK / 8; ++s) umma_tf32_ts(d, a + 8u * s, d0 + s * step, id, hi ? s > 0 : 1);
+      umma_commit(b_mma);
+    };
+    ColTile<DK> R;
+    auto state_ptr = [&](const Item& x, int h) {
+      return p.state + (static_cast<size_t>(x.bl) * p.Hv + h) * DK * DV + c;
+    };
+
+    int k = g;
+    Item cur = item_at(k);
+    if (cur.it < n_items) {
+      // prologue: everything the first head needs
+      issue_kq(cur);
+      load_item_regs(cur);
+      issue_rows(cur, cur.h0);
+      const int lp0 = lp_nx > 0 ? lp_nx : 0;
+      issue_pend(cur, cur.h0, min(kPFold, lp0), pth_nx);   // (warp 0: c = lane, entry c)
+      load_head_regs(cur, cur.h0, lp0, pth_nx);
+      R.load(state_ptr(cur, cur.h0), DV);
+      prefetch_ahead(k, 0, 1);
+    }
+    while (ok && cur.it < n_items) {
+      // ---------------------------- item start ----------------------------
+      // a give-up in this launch, or a timeout left set by an earlier one: no further work (and no writes)
+      ok = group_and(gid, *abortw == 0);
+      if (!ok) break;
+      if (c < lay.words()) rec[c] = rw0;   // (the record is shorter than the group: the path follows it)
+      if (c + kPGroup < lay.words()) rec[c + kPGroup] = rw1;
+      if (c < n_max) spath[c] = pth_nx;
+      const int pth_cur = pth_nx;
+      const int Lraw = lp_nx;
+      const int Lp = Lraw > 0 ? Lraw : 0;
+      group_sync(gid);
+      const int n = rec[0];
+      bool item_ok = n >= 1 && n <= n_max && Lraw >= 0;
+      if (item_ok && c < n) item_ok = c == 0 ? parent[0] == -1 : (parent[c] >= 0 && parent[c] < c);
+      item_ok = group_and(gid, item_ok);
+      if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
+      ok = group_and(gid, mbar_wait_ab(b_kq, ph_kq, abortw));
+      if (!ok) break;   // (still armed: the drain below waits for the copy)
+      ph_kq ^= 1;
+      armed_kq = false;
+      const int NB = (n + 7) & ~7;
+      if (item_ok) {
+        // [k | q] operand, tf32 high rows r < 2 NB and low rows 2 NB + r; a warp step covers 8 rows x 4
+        // chunks with the chunk index rotated by the row, so reads and writes each hit distinct banks
+        const int kbn = (KC + 7) / 8;
+        const int steps = (2 * NB / 8) * kbn * 2;
+        const int e = lane & 7, qd = lane >> 3;
+        for (int s = wq; s < steps; s += 4) {
+          const int rb8 = s / (2 * kbn), kb = (s >> 1) % kbn, hh = s & 1;
+          const int r = 8 * rb8 + e;
+          const int kc = 8 * kb + ((e + qd + 4 * hh) & 7);
+          if (kc < KC) {
+            const bool isq = r >= NB;
+            const int node = isq ? r - NB : r;
+            float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (node < n) x4 = *reinterpret_cast<const float4*>(stg + ((isq ? n_max : 0) + node) * DK + 4 * kc);
+            float4 hi, lo;
+            hi.x = tf32_round(x4.x); lo.x = tf32_round(x4.x - hi.x);
+            hi.y = tf32_round(x4.y); lo.y = tf32_round(x4.y - hi.y);
+            hi.z = tf32_round(x4.z); lo.z = tf32_round(x4.z - hi.z);
+            hi.w = tf32_round(x4.w); lo.w = tf32_round(x4.w - hi.w);
+            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
+            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+          }
+        }
+        fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
+        // depths and pair offsets (warp 0, a lane per node), then every node's ancestors
+        if (wq == 0) {
+          int d = 0;
+          if (lane < n)
+            for (int v = lane; v > 0; v = parent[v]) ++d;
+          int incl = d;
+#pragma unroll
+          for (int m = 1; m < 32; m <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, m);
+            if (lane >= m) incl += y;
+          }
+          if (lane < n) {
+            dep[lane] = d;
+            coff[lane] = incl - d;
+            int i = incl - d;
+            for (int v = parent[lane]; v >= 0; v = parent[v], ++i) {
+              ranc[i] = v;
+              ptn[i] = lane;
+            }
+          }
+          if (lane == n - 1) coff[n] = incl;
+        }
+      }
+      group_sync(gid);
+      if (item_ok) {
+        // Gram coefficients, a warp per ancestor pair (and per node for H_tt), lanes along d_k
+        const int np = coff[n];
+        for (int job = wq; job < np + n; job += 4) {
+          const bool diag = job >= np;
+          const int t = diag ? job - np : ptn[job];
+          const int s = diag ? t : ranc[job];
+          const float* kt = stg + t * DK;
+          const float* qt = stg + (n_max + t) * DK;
+          const float* ks = stg + s * DK;
+          float sg = 0.f, sh = 0.f;
+#pragma unroll
+          for (int e2 = lane; e2 < DK; e2 += 32) {
+            sg = fmaf(kt[e2], ks[e2], sg);
+            sh = fmaf(qt[e2], ks[e2], sh);
+          }
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1) {
+            sg += __shfl_xor_sync(FULL, sg, m);
+            sh += __shfl_xor_sync(FULL, sh, m);
+          }
+          if (lane == 0) {
+            if (diag) hd[t] = sh;
+            else gh[job] = make_float2(sg, sh);
+          }
+        }
+      }
+      fence_proxy_async();   // staging reads done before the next item's copies overwrite it
+      group_sync(gid);
+      // the next item of this group: its k and q rows, record and path
+      Item nxt = item_at(k + NG);
+      if (nxt.it < n_items) {
+        issue_kq(nxt);
+        load_item_regs(nxt);
+      }
+
+      // ---------------------------- heads of the item ----------------------------
+      for (int j = 0; j < hpi && ok; ++j) {
+        const int h = cur.h0 + j;
+        const size_t nrow0 = static_cast<size_t>(cur.bl) * n_max;
+        // the head after this one (same item, or the next item's first)
+        const bool nx_same = j + 1 < hpi;
+        const bool has_nx = nx_same || nxt.it < n_items;
+        const Item& nxi = nx_same ? cur : nxt;
+        const int nxh = nx_same ? h + 1 : nxt.h0;
+        const int nx_lp = nx_same ? Lp : (lp_nx > 0 ? lp_nx : 0);
+        prefetch_ahead(k, j, 2);   // the state two heads ahead into L2
+        // head tables from the registers loaded during the previous head
+        if (item_ok && c < n) {
+          hsc[c] = make_float4(expf(ra), rb, 0.f, 0.f);
+          p.a_out[(nrow0 + c) * p.Hv + h] = ra;   // the bank's log-gate, exact
+        }
+        if (c < Lp) pgt[c] = rpg;
+        group_sync(gid);
+
+        // ---- 1. fold of the pending path (the chain kernel's element operations and materialisation points)
+        float gam = 1.f;
+        for (int f0 = 0; f0 < Lp; f0 += kPFold) {
+          const int fn = min(kPFold, Lp - f0);
+          ok = group_and(gid, mbar_wait_ab(b_pend, ph_pend, abortw));
+          if (!ok) break;
+          ph_pend ^= 1;
+          armed_pend = false;
+          if (item_ok) {
+            for (int i = 0; i < fn; ++i) {
+              if (spath[f0 + i] & kPathHeadFlag) {
+                R.materialise(gam);
+                gam = 1.f;
+              }
+              gam = fold_node(R, pk + i * DK, gam * pgt[f0 + i], pu[i * DV + c]);
+            }
+          }
+          fence_proxy_async();
+          group_sync(gid);
+          if (f0 + kPFold < Lp) {
+            const int pe = f0 + kPFold + lane < n_max ? spath[f0 + kPFold + lane] : 0;
+            issue_pend(cur, h, min(kPFold, Lp - f0 - kPFold), pe);
+          }
+        }
+        if (!ok) break;
+        float* st = p.state + (static_cast<size_t>(cur.bl) * p.Hv + h) * DK * DV + c;
+        if (item_ok && Lp > 0) {
+          R.materialise(gam);
+          R.store(st, DV);
+        }
+        // the pending buffers are free: the next head's first chunk
+        if (has_nx) {
+          const int pe = nx_same ? (lane < n_max ? spath[lane] : 0) : pth_nx;   // (warp 0: c = lane)
+          issue_pend(nxi, nxh, min(kPFold, nx_lp), pe);
+        }
+
+        // ---- 2. A = T0^T, high part, and its product with all 4 NB operand rows
+        if (item_ok) {
+#pragma unroll
+          for (int q = 0; q < DK / 16; ++q) {
+            float v[16];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float2 e2 = unpack2(R.T[8 * q + jj]);
+              v[2 * jj] = tf32_round(e2.x);
+              v[2 * jj + 1] = tf32_round(e2.y);
+            }
+            tmem_st16(tA + 16u * q, v);
+          }
+          tmem_wait_st();
+        }
+        tmem_fence_before();
+        group_sync(gid);
+        if (item_ok) {
+          if (c == 0) {
+            tmem_fence_after();
+            issue_mma(true, NB);
+          }
+          armed_mma = true;
+        }
+
+        // ---- 3. this head's coefficients: a thread of warp 1 per node walks its ancestors (rho by products,
+        // no division), A_ts = beta_t rho_ts G_ts and C_ts = rho_ts H_ts into the pair table
+        if (item_ok && wq == 1 && lane < n) {
+          const int t = lane;
+          const float4 sc = hsc[t];
+          float prod = 1.f;
+          int v = t, i = coff[t];
+          while (v > 0) {
+            prod *= hsc[v].x;
+            v = parent[v];
+            const float2 q2 = gh[i];
+            ptab[i] = make_float4(sc.y * prod * q2.x, prod * q2.y, __int_as_float(v * DV), 0.f);
+            ++i;
+          }
+          const float gam_t = prod * hsc[0].x;
+          reinterpret_cast<float*>(hsc + t)[2] = sc.y * gam_t;
+          reinterpret_cast<float*>(hsc + t)[3] = gam_t;
+        }
+
+        // ---- the low part of A once the high product has read it, and its product with the high rows
+        if (item_ok) {
+          ok = group_and(gid, mbar_wait_ab(b_mma, ph_mma, abortw));
+          if (!ok) break;
+          ph_mma ^= 1;
+          armed_mma = false;
+          tmem_fence_after();
+#pragma unroll
+          for (int q = 0; q < DK / 16; ++q) {
+            float v[16];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float2 e2 = unpack2(R.T[8 * q + jj]);
+              v[2 * jj] = tf32_round(e2.x - tf32_round(e2.x));
+              v[2 * jj + 1] = tf32_round(e2.y - tf32_round(e2.y));
+            }
+            tmem_st16(tA + 16u * q, v);
+          }
+          tmem_wait_st();
+          tmem_fence_before();
+          group_sync(gid);   // also publishes the pair table and Gamma
+          if (c == 0) {
+            tmem_fence_after();
+            issue_mma(false, NB);
+          }
+          armed_mma = true;
+        }
+
+        // ---- 4. the registers are free: the next head's state column and gates (after the boundary
+        // replay instead, when boundary states are stored, since it replays from T0 in these registers)
+        if (!p.boundary_out && has_nx) {
+          R.load(state_ptr(nxi, nxh), DV);
+          load_head_regs(nxi, nxh, nx_lp, nx_same ? pth_cur : pth_nx);
+        }
+
+        // ---- 5. epilogue: forward substitution down the nodes, column c
+        ok = group_and(gid, mbar_wait_ab(b_rows, ph_rows, abortw));
+        if (!ok) break;
+        ph_rows ^= 1;
+        armed_rows = false;
+        if (item_ok) {
+          ok = group_and(gid, mbar_wait_ab(b_mma, ph_mma, abortw));
+          if (!ok) break;
+          ph_mma ^= 1;
+          armed_mma = false;
+          tmem_fence_after();
+          const size_t ostride = static_cast<size_t>(p.Hv) * DV;
+          float* o_col = p.out_o + (nrow0 * p.Hv + h) * DV + c;
+          float* u_col = p.u_out + (nrow0 * p.Hv + h) * DV + c;
+          float* vcol = vbuf + c;
+          for (int t0 = 0; t0 < n; t0 += 8) {
+            float k1[8], k2[8], q1[8], q2[8];
+            tmem_ld8(tD + static_cast<uint32_t>(t0), k1);
+            tmem_ld8(tD + static_cast<uint32_t>(2 * NB + t0), k2);
+            tmem_ld8(tD + static_cast<uint32_t>(NB + t0), q1);
+            tmem_ld8(tD + static_cast<uint32_t>(3 * NB + t0), q2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int t = t0 + jj;
+              if (t < n) {
+                const float4 sc = hsc[t];
+                float u = fmaf(-sc.z, k1[jj] + k2[jj], sc.y * vcol[t * DV]);
+                float oc = 0.f;
+                const int i1 = coff[t + 1];
+                for (int i = coff[t]; i < i1; ++i) {
+                  const float4 e4 = ptab[i];
+                  const float us = vcol[__float_as_int(e4.z)];
+                  u = fmaf(-e4.x, us, u);
+                  oc = fmaf(e4.y, us, oc);
+                }
+                const float o = fmaf(hd[t], u, fmaf(sc.w, q1[jj] + q2[jj], oc));
+                vcol[t * DV] = u;
+                u_col[t * ostride] = u;
+                o_col[t * ostride] = o;
+              }
+            }
+          }
+        }
+        tmem_fence_before();
+
+        // ---- boundary states on request, replayed from T0 with the fold's operations and materialisation
+        // points (k rows from the bank, u rows from shared memory), so a later fold reproduces them bit for bit
+        if (p.boundary_out) {
+          if (item_ok) {
+            for (int node = 0; node < n; ++node) {
+              const int slot = bslot[node];
+              if (slot < 0 || slot >= p.nb_max) continue;
+              int m = 0;
+              for (int v = node; v >= 0; v = parent[v]) ++m;
+              R.load(st, DV);   // T0: the committed state written above, or the input state when nothing folded
+              float gg = 1.f;
+              for (int i = 0; i < m; ++i) {
+                int v = node;   // the i-th node of the root path, root first
+                for (int s2 = 0; s2 < m - 1 - i; ++s2) v = parent[v];
+                if (i > 0 && (nflags[parent[v]] & kNodeMaterialised)) {
+                  R.materialise(gg);
+                  gg = 1.f;
+                }
+                gg = fold_node(R, p.k_in + ((nrow0 + v) * p.Hk + cur.kh) * DK, gg * hsc[v].x, vbuf[v * DV + c]);
+              }
+              R.materialise(gg);
+              R.store(p.boundary + ((static_cast<size_t>(cur.bl) * p.nb_max + slot) * p.Hv + h) * DK * DV + c, DV);
+            }
+          }
+          if (has_nx) {
+            R.load(state_ptr(nxi, nxh), DV);
+            load_head_regs(nxi, nxh, nx_lp, nx_same ? pth_cur : pth_nx);
+          }
+        }
+        fence_proxy_async();   // the u rows written into vbuf, before the next copy overwrites it
+        group_sync(gid);
+        if (has_nx) issue_rows(nxi, nxh);
+      }
+      k += NG;
+      cur = nxt;
+    }
+    // ---- end of the group: on a give-up every role stops; copies and MMAs still in flight complete
+    // before the shared and tensor memory are released
+    if (!ok && c == 0) {
+      *abortw = 1;
+      device_error(p.err, GDN_DEVERR_TIMEOUT, cur.it < n_items ? cur.b : 0);
+    }
+    if (armed_kq) mbar_wait(b_kq, ph_kq);
+    if (armed_rows) mbar_wait(b_rows, ph_rows);
+    if (armed_pend) mbar_wait(b_pend, ph_pend);
+    if (armed_mma) mbar_wait(b_mma, ph_mma);
+  }
+  __syncwarp();
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tmem_fence_after();
+    tmem_dealloc(tbase, NG * 256);
+  }
+}
+
+template <int DK, typename InT, int NG>
+cudaError_t launch_tcp_t(const VerifyParams& p, cudaStream_t s) {
+  const PLayout L{p.n_max, DK};
+  // at least half an SM's shared memory, so one CTA (and one tensor-memory allocation) per SM
+  const size_t smem = L.bytes(NG) > 116 * 1024 ? static_cast<size_t>(L.bytes(NG)) : 116 * 1024;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  auto kern = ut_tcp_verify_kernel<DK, InT, NG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // an item is a k-head with its R v-heads when there are enough of them for every group of every SM,
+  // else a single v-head
+  const long long kheads = static_cast<long long>(p.B) * p.layers * p.Hk;
+  const int hpi = kheads >= static_cast<long long>(sms) * NG ? p.R : 1;
+  const long long items = static_cast<long long>(p.B) * p.layers * p.Hv / hpi;
+  if (items > 0x7fffffffll) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  kern<<<grid, NG * kPGroup, smem, s>>>(p, static_cast<int>(items), hpi);
+  return cudaGetLastError();
+}
+
+template <int DK, typename InT>
+cudaError_t launch_tcp_groups(const VerifyParams& p, cudaStream_t s) {
+  const PLayout L{p.n_max, DK};
+  if (L.bytes(2) <= 227 * 1024) return launch_tcp_t<DK, InT, 2>(p, s);
+  return launch_tcp_t<DK, InT, 1>(p, s);
+}
+
+template <typename InT>
+cudaError_t launch_tcp_dtype(const VerifyParams& p, cudaStream_t s) {
+  switch (p.dk) {
+    case 32: return launch_tcp_groups<32, InT>(p, s);
+    case 64: return launch_tcp_groups<64, InT>(p, s);
+    case 128: return launch_tcp_groups<128, InT>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool verify_tcp_supported(int dk, int dv, int n_max) {
+  if (dv != kPDv || !(dk == 32 || dk == 64 || dk == 128) || n_max < 1 || n_max > kPMaxNodes) return false;
+  return PLayout{n_max, dk}.bytes(1) <= 227 * 1024;
+}
+
+cudaError_t launch_verify_tcp(const VerifyParams& p, cudaStream_t s) {
+  if (!verify_tcp_supported(p.dk, p.dv, p.n_max)) return cudaErrorInvalidValue;
+  if (p.in_dtype == GDN_DTYPE_BF16) return launch_tcp_dtype<__nv_bfloat16>(p, s);
+  return launch_tcp_dtype<float>(p, s);
+}
+
+}  // namespace gdn

@@ -252,6 +252,7 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
 #define GDN_VERIFY_BOUNDARY_SCRATCH 1   /* boundary_states is scratch, not output */
 #define GDN_VERIFY_CHAIN_WALK 2         /* walk the heavy-light chains instead of the tree-masked UT form */
 #define GDN_VERIFY_UT_SIMT 4            /* UT form on the CUDA cores even where the tensor-core kernel applies */
+#define GDN_VERIFY_TC_PER_HEAD 8        /* tensor-core UT form with one CTA per v-head instead of the persistent kernel */
 
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify -- fold the pending path, then verify a batch of trees.

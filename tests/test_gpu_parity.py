@@ -27,15 +27,17 @@ def _np(t):
     return t.detach().cpu().numpy().astype(np.float64)
 
 
-# verify kernels: "ut" the default dispatch (the tree-masked UT form, on the tensor cores where d_v = 128
-# and n_max <= 32), "simt" the UT form on the CUDA cores, "walk" the heavy-light chain walk
-KERNELS = ["ut", "simt", "walk"]
+# verify kernels: "ut" the default dispatch (the tree-masked UT form, on the tensor cores in the persistent
+# kernel where d_v = 128 and n_max <= 32), "tc1" the tensor-core UT form with a CTA per v-head, "simt" the UT
+# form on the CUDA cores, "walk" the heavy-light chain walk
+KERNELS = ["ut", "tc1", "simt", "walk"]
 
 
 def set_kernel(plan, kernel):
     assert kernel in KERNELS, kernel
     plan.chain_walk = plan.chain_walk or kernel == "walk"
     plan.ut_simt = plan.ut_simt or kernel == "simt"
+    plan.tc_per_head = plan.tc_per_head or kernel == "tc1"
     return plan
 
 
@@ -119,7 +121,7 @@ def test_tiny_bypass_mode():
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_head_shapes_and_gqa(dk, dv, kernel):
     # d_k != d_v catches a transposed state; Hv = 3 Hk checks the v-head -> k-head map
-    if kernel == "simt" and dv != 128:
+    if kernel in ("simt", "tc1") and dv != 128:
         pytest.skip("the default UT dispatch already runs the CUDA-core kernel for this d_v")
     w = S.workload(1).replace(Hk=2, Hv=6, dk=dk, dv=dv, steps=3, tree="random", budget=12, n_max=12, path_max=12)
     run_parity(w, kernel=kernel)
@@ -131,7 +133,7 @@ def test_ragged_batch_and_degenerate_trees(heads, kernel):
     # per-request tree sizes 1 .. n_max, a single-node tree, a full chain, L = 0 and L = n commits;
     # with 128-wide heads the UT form runs on the tensor cores, whose node padding these sizes cross
     n_max = 16 if heads == "tiny" else 32
-    if heads == "tiny" and kernel == "simt":
+    if heads == "tiny" and kernel in ("simt", "tc1"):
         pytest.skip("the default UT dispatch already runs the CUDA-core kernel for these heads")
     w = S.workload(1).replace(B=5, layers=2, n_max=n_max, steps=3, tree="random", budget=n_max, path_max=n_max)
     if heads == "d128":
@@ -182,7 +184,7 @@ def test_deep_light_depth_spills_stashes_to_hbm(cfg, kernel):
         ts = [binary_tree(31), binary_tree(n_max), S.random_tree(n_max, rng)]
         trees.append(ts)
         paths.append([S.random_walk_path(t, rng, max_len=n_max) for t in ts])
-    if cfg == 1 and kernel == "simt":
+    if cfg == 1 and kernel in ("simt", "tc1"):
         pytest.skip("the default UT dispatch already runs the CUDA-core kernel for these heads")
     run_parity(w, plan=WorkloadPlan(w, trees, paths), kernel=kernel)
 
