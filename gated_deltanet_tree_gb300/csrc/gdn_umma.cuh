@@ -16,8 +16,8 @@
 //     bytes apart;
 //   - one instruction covers K = 8 (two core matrices along K).
 // A tf32 operand keeps 10 of fp32's 23 mantissa bits.  Products that need fp32
-// accuracy split each operand as x = hi + lo with hi = tf32(x), lo = tf32(x - hi)
-// and accumulate hi*hi + hi*lo + lo*hi (the lo*lo term is below fp32 rounding).
+// accuracy split each operand as x = hi + lo (tf32_hi / tf32_lo below) and
+// accumulate hi*hi + hi*lo + lo*hi (the lo*lo term is below fp32 rounding).
 #pragma once
 #include <cstdint>
 
@@ -116,12 +116,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_tf32(int m, int n) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
-// tf32 rounding (to nearest, ties away from zero) kept in an fp32 register.
-__device__ __forceinline__ float tf32_round(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
+// The two-term tf32 split x = hi + lo: hi keeps the sign, the exponent and the top 10 fraction bits of x
+// (the low 13 fraction bits cleared, so it is a tf32 value exactly), lo = x - hi is exact in fp32 and holds
+// at most the remaining 13 bits; read as tf32 by the tensor cores it loses at most its lowest bits, an error
+// below 2^-21 |x|.  Two integer/fp ops instead of two conversions and a subtraction.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+__device__ __forceinline__ float tf32_lo(float x) { return x - tf32_hi(x); }
 // D (+)= A B^T with A in tensor memory.
 __device__ __forceinline__ void umma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, int accumulate) {
   asm volatile(

@@ -277,10 +277,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) ut_tc_verify_kernel(VerifyParam
           float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
           if (node < n) x = *reinterpret_cast<const float4*>(sm + L.kq(node) + (isq ? DK : 0) + 4 * kc);
           float4 hi, lo;
-          hi.x = tf32_round(x.x); lo.x = tf32_round(x.x - hi.x);
-          hi.y = tf32_round(x.y); lo.y = tf32_round(x.y - hi.y);
-          hi.z = tf32_round(x.z); lo.z = tf32_round(x.z - hi.z);
-          hi.w = tf32_round(x.w); lo.w = tf32_round(x.w - hi.w);
+          hi.x = tf32_hi(x.x); lo.x = tf32_lo(x.x);
+          hi.y = tf32_hi(x.y); lo.y = tf32_lo(x.y);
+          hi.z = tf32_hi(x.z); lo.z = tf32_lo(x.z);
+          hi.w = tf32_hi(x.w); lo.w = tf32_lo(x.w);
           *reinterpret_cast<float4*>(sm + L.bq() + kc * lbo4 + 4 * r) = hi;
           *reinterpret_cast<float4*>(sm + L.bq() + kc * lbo4 + 4 * (2 * NB + r)) = lo;
         }
@@ -434,8 +434,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) ut_tc_verify_kernel(VerifyParam
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float2 e = unpack2(R.T[8 * q + j]);
-        v[2 * j] = tf32_round(e.x);
-        v[2 * j + 1] = tf32_round(e.y);
+        v[2 * j] = tf32_hi(e.x);
+        v[2 * j + 1] = tf32_hi(e.y);
       }
       tmem_st16(tlane + static_cast<uint32_t>(row0 + 16 * q), v);
     }
@@ -483,8 +483,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) ut_tc_verify_kernel(VerifyParam
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float2 e = unpack2(R.T[8 * q + j]);
-        v[2 * j] = tf32_round(e.x - tf32_round(e.x));
-        v[2 * j + 1] = tf32_round(e.y - tf32_round(e.y));
+        v[2 * j] = tf32_lo(e.x);
+        v[2 * j + 1] = tf32_lo(e.y);
       }
       tmem_st16(tlane + static_cast<uint32_t>(row0 + 16 * q), v);
     }

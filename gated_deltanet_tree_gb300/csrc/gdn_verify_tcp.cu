@@ -126,6 +126,12 @@ __device__ __forceinline__ float fold_node(ColTile<NR>& R, const float* krows, f
   return gam1;
 }
 
+__device__ __forceinline__ float tmem_ld1(uint32_t ta) {
+  float v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=f"(v) : "r"(ta) : "memory");
+  return v;
+}
+
 // Shared-memory layout in bytes: NG group regions, then the CTA's barriers and words.
 struct PLayout {
   int n_max, dk;
@@ -137,7 +143,8 @@ struct PLayout {
   __host__ __device__ int opnd() const { return 0; }                                 // [dk/4][4 NB][16 B] operand
   __host__ __device__ int stg() const { return opnd() + 4 * nbm() * dk * 4; }         // [2][n_max][dk] k, q rows
   __host__ __device__ int vbuf() const { return stg() + 2 * n_max * dk * 4; }         // [n_max][128] v, then u
-  __host__ __device__ int pk() const { return vbuf() + n_max * kPDv * 4; }            // [kPFold][dk] pending k
+  __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [n_max][128] u by depth
+  __host__ __device__ int pk() const { return stk() + n_max * kPDv * 4; }             // [kPFold][dk] pending k
   __host__ __device__ int pu() const { return pk() + kPFold * dk * 4; }               // [kPFold][128] pending u
   __host__ __device__ int ptab() const { return pu() + kPFold * kPDv * 4; }           // [pairs] (A, C, s dv, -)
   __host__ __device__ int hsc() const { return ptab() + a16(pairs() * 16); }          // [n_max] (g, beta, bG, G)
@@ -200,6 +207,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
     float* opnd = reinterpret_cast<float*>(gb + L.opnd());
     float* stg = reinterpret_cast<float*>(gb + L.stg());
     float* vbuf = reinterpret_cast<float*>(gb + L.vbuf());
+    float* stk = reinterpret_cast<float*>(gb + L.stk());
     float* pk = reinterpret_cast<float*>(gb + L.pk());
     float* pu = reinterpret_cast<float*>(gb + L.pu());
     float4* ptab = reinterpret_cast<float4*>(gb + L.ptab());
@@ -378,10 +386,10 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
             float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (node < n) x4 = *reinterpret_cast<const float4*>(stg + ((isq ? n_max : 0) + node) * DK + 4 * kc);
             float4 hi, lo;
-            hi.x = tf32_round(x4.x); lo.x = tf32_round(x4.x - hi.x);
-            hi.y = tf32_round(x4.y); lo.y = tf32_round(x4.y - hi.y);
-            hi.z = tf32_round(x4.z); lo.z = tf32_round(x4.z - hi.z);
-            hi.w = tf32_round(x4.w); lo.w = tf32_round(x4.w - hi.w);
+            hi.x = tf32_hi(x4.x); lo.x = tf32_lo(x4.x);
+            hi.y = tf32_hi(x4.y); lo.y = tf32_lo(x4.y);
+            hi.z = tf32_hi(x4.z); lo.z = tf32_lo(x4.z);
+            hi.w = tf32_hi(x4.w); lo.w = tf32_lo(x4.w);
             *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
             *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
           }
@@ -411,31 +419,53 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         }
       }
       group_sync(gid);
+      // the epilogue visits the nodes in the schedule's walk order (depth first, a node after its parent), so
+      // the u values on a node's root path are the entries of a per-column stack indexed by depth.  Lane w of
+      // every warp holds walk position w: node | depth << 8 | pair offset << 16.  The order is checked: every
+      // node once, the root first, the depth rising by at most one per step, and each node's parent the last
+      // node visited one level up (so the stack always holds the current node's root path).
+      int wpack = 0;
       if (item_ok) {
-        // Gram coefficients, a warp per ancestor pair (and per node for H_tt), lanes along d_k
+        const int w = lane;
+        const int t = w < n ? (rec[lay.ops() + w] & kOpNode) : 0;
+        const bool in = w < n && t < n;
+        const int d = in ? dep[t] : 0;
+        bool good = w >= n || in;
+        const unsigned seen = __reduce_or_sync(FULL, in ? 1u << t : 0u);
+        good = good && __popc(seen) == n && (w != 0 || t == 0);
+        if (in && w > 0) {   // the nearest earlier position one level up must hold the parent
+          const int tp = rec[lay.ops() + w - 1] & kOpNode;
+          good = good && tp < n && d <= dep[min(tp, n - 1)] + 1;
+          int q = w - 1;
+          auto node_at = [&](int pos) { return min(rec[lay.ops() + pos] & kOpNode, n - 1); };
+          while (q > 0 && dep[node_at(q)] != d - 1) --q;
+          good = good && node_at(q) == parent[t] && dep[node_at(q)] == d - 1;
+        }
+        wpack = t | (d << 8) | ((in ? coff[t] : 0) << 16);
+        item_ok = group_and(gid, good);
+        if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
+      }
+      if (item_ok) {
+        // Gram coefficients, a thread per ancestor pair (and per node for H_tt); the 16-byte chunks are read
+        // in an order rotated by the job, so the threads of a warp hit distinct banks
         const int np = coff[n];
-        for (int job = wq; job < np + n; job += 4) {
+        for (int job = c; job < np + n; job += kPGroup) {
           const bool diag = job >= np;
           const int t = diag ? job - np : ptn[job];
           const int s = diag ? t : ranc[job];
-          const float* kt = stg + t * DK;
-          const float* qt = stg + (n_max + t) * DK;
-          const float* ks = stg + s * DK;
-          float sg = 0.f, sh = 0.f;
-#pragma unroll
-          for (int e2 = lane; e2 < DK; e2 += 32) {
-            sg = fmaf(kt[e2], ks[e2], sg);
-            sh = fmaf(qt[e2], ks[e2], sh);
+          const float4* kt = reinterpret_cast<const float4*>(stg + t * DK);
+          const float4* qt = reinterpret_cast<const float4*>(stg + (n_max + t) * DK);
+          const float4* ks = reinterpret_cast<const float4*>(stg + s * DK);
+          float sg[2] = {0.f, 0.f}, sh[2] = {0.f, 0.f};   // two partial sums each: shorter dependency chains
+#pragma unroll 8
+          for (int q = 0; q < KC; ++q) {
+            const int kc = (q + job) & (KC - 1);
+            const float4 a = kt[kc], b = qt[kc], e = ks[kc];
+            sg[q & 1] += fmaf(a.x, e.x, a.y * e.y) + fmaf(a.z, e.z, a.w * e.w);
+            sh[q & 1] += fmaf(b.x, e.x, b.y * e.y) + fmaf(b.z, e.z, b.w * e.w);
           }
-#pragma unroll
-          for (int m = 16; m > 0; m >>= 1) {
-            sg += __shfl_xor_sync(FULL, sg, m);
-            sh += __shfl_xor_sync(FULL, sh, m);
-          }
-          if (lane == 0) {
-            if (diag) hd[t] = sh;
-            else gh[job] = make_float2(sg, sh);
-          }
+          if (diag) hd[t] = sh[0] + sh[1];
+          else gh[job] = make_float2(sg[0] + sg[1], sh[0] + sh[1]);
         }
       }
       fence_proxy_async();   // staging reads done before the next item's copies overwrite it
@@ -492,10 +522,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         }
         if (!ok) break;
         float* st = p.state + (static_cast<size_t>(cur.bl) * p.Hv + h) * DK * DV + c;
-        if (item_ok && Lp > 0) {
-          R.materialise(gam);
-          R.store(st, DV);
-        }
+        if (item_ok && Lp > 0) R.materialise(gam);
         // the pending buffers are free: the next head's first chunk
         if (has_nx) {
           const int pe = nx_same ? (lane < n_max ? spath[lane] : 0) : pth_nx;   // (warp 0: c = lane)
@@ -510,8 +537,8 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
               const float2 e2 = unpack2(R.T[8 * q + jj]);
-              v[2 * jj] = tf32_round(e2.x);
-              v[2 * jj + 1] = tf32_round(e2.y);
+              v[2 * jj] = tf32_hi(e2.x);
+              v[2 * jj + 1] = tf32_hi(e2.y);
             }
             tmem_st16(tA + 16u * q, v);
           }
@@ -526,6 +553,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           }
           armed_mma = true;
         }
+        if (item_ok && Lp > 0) R.store(st, DV);   // the committed state, written once, while the product runs
 
         // ---- 3. this head's coefficients: a thread of warp 1 per node walks its ancestors (rho by products,
         // no division), A_ts = beta_t rho_ts G_ts and C_ts = rho_ts H_ts into the pair table
@@ -559,8 +587,8 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
               const float2 e2 = unpack2(R.T[8 * q + jj]);
-              v[2 * jj] = tf32_round(e2.x - tf32_round(e2.x));
-              v[2 * jj + 1] = tf32_round(e2.y - tf32_round(e2.y));
+              v[2 * jj] = tf32_lo(e2.x);
+              v[2 * jj + 1] = tf32_lo(e2.y);
             }
             tmem_st16(tA + 16u * q, v);
           }
@@ -596,33 +624,30 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           float* o_col = p.out_o + (nrow0 * p.Hv + h) * DV + c;
           float* u_col = p.u_out + (nrow0 * p.Hv + h) * DV + c;
           float* vcol = vbuf + c;
-          for (int t0 = 0; t0 < n; t0 += 8) {
-            float k1[8], k2[8], q1[8], q2[8];
-            tmem_ld8(tD + static_cast<uint32_t>(t0), k1);
-            tmem_ld8(tD + static_cast<uint32_t>(2 * NB + t0), k2);
-            tmem_ld8(tD + static_cast<uint32_t>(NB + t0), q1);
-            tmem_ld8(tD + static_cast<uint32_t>(3 * NB + t0), q2);
-            tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int t = t0 + jj;
-              if (t < n) {
-                const float4 sc = hsc[t];
-                float u = fmaf(-sc.z, k1[jj] + k2[jj], sc.y * vcol[t * DV]);
-                float oc = 0.f;
-                const int i1 = coff[t + 1];
-                for (int i = coff[t]; i < i1; ++i) {
-                  const float4 e4 = ptab[i];
-                  const float us = vcol[__float_as_int(e4.z)];
-                  u = fmaf(-e4.x, us, u);
-                  oc = fmaf(e4.y, us, oc);
-                }
-                const float o = fmaf(hd[t], u, fmaf(sc.w, q1[jj] + q2[jj], oc));
-                vcol[t * DV] = u;
-                u_col[t * ostride] = u;
-                o_col[t * ostride] = o;
-              }
+          float* sc_col = stk + c;
+          for (int w = 0; w < n; ++w) {
+            const int pkw = __shfl_sync(FULL, wpack, w);
+            const int t = pkw & 0xFF, d = (pkw >> 8) & 0xFF, i0 = pkw >> 16;
+            const uint32_t tc = tD + static_cast<uint32_t>(t);
+            const float k1 = tmem_ld1(tc), k2 = tmem_ld1(tc + 2u * NB);
+            const float q1 = tmem_ld1(tc + static_cast<uint32_t>(NB)), q2 = tmem_ld1(tc + 3u * NB);
+            const float4 sc = hsc[t];
+            const float vt = vcol[t * DV], htt = hd[t];
+            float su = 0.f, so = 0.f;
+#pragma unroll 4
+            for (int m = 0; m < d; ++m) {   // m-th ancestor (parent first) sits at depth d - 1 - m
+              const float4 e4 = ptab[i0 + m];
+              const float us = sc_col[(d - 1 - m) * DV];
+              su = fmaf(e4.x, us, su);
+              so = fmaf(e4.y, us, so);
             }
+            tmem_wait_ld();
+            const float u = fmaf(-sc.z, k1 + k2, sc.y * vt) - su;
+            const float o = fmaf(htt, u, fmaf(sc.w, q1 + q2, so));
+            sc_col[d * DV] = u;
+            vcol[t * DV] = u;   // the u rows by node, for the boundary replay
+            u_col[t * ostride] = u;
+            o_col[t * ostride] = o;
           }
         }
         tmem_fence_before();
