@@ -104,7 +104,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t ta, float (&v)[8]) {
 }
 
 // ColTile::advance (one node of the gated delta rule on the lazily decayed column) with the same operands
-// in the same order, so the results are bit-identical; the k row is read 16 values at a time, with a
+// in the same order, so the results are bit-identical; the k row is read 32 values at a time, with a
 // compiler barrier between the pieces, so a whole 128-row column plus its k row never need registers at once.
 template <int NR>
 __device__ __forceinline__ float fold_node(ColTile<NR>& R, const float* krows, float gam1, float u) {
@@ -121,7 +121,7 @@ __device__ __forceinline__ float fold_node(ColTile<NR>& R, const float* krows, f
     const ulonglong2 kk = k4[j4];
     R.T[2 * j4 + 0] = fma2(kk.x, u2, R.T[2 * j4 + 0]);
     R.T[2 * j4 + 1] = fma2(kk.y, u2, R.T[2 * j4 + 1]);
-    if ((j4 & 3) == 3) asm volatile("" ::: "memory");
+    if ((j4 & 7) == 7) asm volatile("" ::: "memory");
   }
   return gam1;
 }
@@ -433,14 +433,23 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         bool good = w >= n || in;
         const unsigned seen = __reduce_or_sync(FULL, in ? 1u << t : 0u);
         good = good && __popc(seen) == n && (w != 0 || t == 0);
-        if (in && w > 0) {   // the nearest earlier position one level up must hold the parent
-          const int tp = rec[lay.ops() + w - 1] & kOpNode;
-          good = good && tp < n && d <= dep[min(tp, n - 1)] + 1;
-          int q = w - 1;
-          auto node_at = [&](int pos) { return min(rec[lay.ops() + pos] & kOpNode, n - 1); };
-          while (q > 0 && dep[node_at(q)] != d - 1) --q;
-          good = good && node_at(q) == parent[t] && dep[node_at(q)] == d - 1;
+        // the parent comes earlier, and no position between the two is shallower than the node (then the
+        // parent's stack entry is still the last one written at its depth when the node is visited)
+        const int pt = in && w > 0 ? parent[t] : -2;
+        bool found = false;
+        int mind = 1 << 20;
+        for (int q = 0; q < 32; ++q) {
+          const int tq = __shfl_sync(FULL, t, q), dq = __shfl_sync(FULL, d, q);
+          if (q < w) {
+            if (tq == pt) {
+              found = true;
+              mind = 1 << 20;
+            } else {
+              mind = min(mind, dq);
+            }
+          }
         }
+        if (in && w > 0) good = good && found && mind >= d;
         wpack = t | (d << 8) | ((in ? coff[t] : 0) << 16);
         item_ok = group_and(gid, good);
         if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
@@ -624,30 +633,50 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           float* o_col = p.out_o + (nrow0 * p.Hv + h) * DV + c;
           float* u_col = p.u_out + (nrow0 * p.Hv + h) * DV + c;
           float* vcol = vbuf + c;
+          // one walk position ahead: the next node's T0^T k and T0^T q (tensor memory) and table values are
+          // in flight while the current node's ancestor sums run; only the stack reads wait on the previous node
           float* sc_col = stk + c;
-          for (int w = 0; w < n; ++w) {
+          struct NodeVals {
+            int t, d, i0;
+            float k1, k2, q1, q2, vt, htt;
+            float4 sc;
+          };
+          auto fetch = [&](int w, NodeVals& x) {
             const int pkw = __shfl_sync(FULL, wpack, w);
-            const int t = pkw & 0xFF, d = (pkw >> 8) & 0xFF, i0 = pkw >> 16;
-            const uint32_t tc = tD + static_cast<uint32_t>(t);
-            const float k1 = tmem_ld1(tc), k2 = tmem_ld1(tc + 2u * NB);
-            const float q1 = tmem_ld1(tc + static_cast<uint32_t>(NB)), q2 = tmem_ld1(tc + 3u * NB);
-            const float4 sc = hsc[t];
-            const float vt = vcol[t * DV], htt = hd[t];
+            x.t = pkw & 0xFF;
+            x.d = (pkw >> 8) & 0xFF;
+            x.i0 = pkw >> 16;
+            const uint32_t tc = tD + static_cast<uint32_t>(x.t);
+            x.k1 = tmem_ld1(tc);
+            x.k2 = tmem_ld1(tc + 2u * NB);
+            x.q1 = tmem_ld1(tc + static_cast<uint32_t>(NB));
+            x.q2 = tmem_ld1(tc + 3u * NB);
+            x.sc = hsc[x.t];
+            x.vt = vcol[x.t * DV];
+            x.htt = hd[x.t];
+          };
+          NodeVals cv;
+          fetch(0, cv);
+          tmem_wait_ld();
+          for (int w = 0; w < n; ++w) {
+            NodeVals nv;
+            if (w + 1 < n) fetch(w + 1, nv);
             float su = 0.f, so = 0.f;
 #pragma unroll 4
-            for (int m = 0; m < d; ++m) {   // m-th ancestor (parent first) sits at depth d - 1 - m
-              const float4 e4 = ptab[i0 + m];
-              const float us = sc_col[(d - 1 - m) * DV];
+            for (int m = 0; m < cv.d; ++m) {   // m-th ancestor (parent first) sits at depth d - 1 - m
+              const float4 e4 = ptab[cv.i0 + m];
+              const float us = sc_col[(cv.d - 1 - m) * DV];
               su = fmaf(e4.x, us, su);
               so = fmaf(e4.y, us, so);
             }
+            const float u = fmaf(-cv.sc.z, cv.k1 + cv.k2, cv.sc.y * cv.vt) - su;
+            const float o = fmaf(cv.htt, u, fmaf(cv.sc.w, cv.q1 + cv.q2, so));
+            sc_col[cv.d * DV] = u;
+            vcol[cv.t * DV] = u;   // the u rows by node, for the boundary replay
+            u_col[cv.t * ostride] = u;
+            o_col[cv.t * ostride] = o;
             tmem_wait_ld();
-            const float u = fmaf(-sc.z, k1 + k2, sc.y * vt) - su;
-            const float o = fmaf(htt, u, fmaf(sc.w, q1 + q2, so));
-            sc_col[d * DV] = u;
-            vcol[t * DV] = u;   // the u rows by node, for the boundary replay
-            u_col[t * ostride] = u;
-            o_col[t * ostride] = o;
+            if (w + 1 < n) cv = nv;
           }
         }
         tmem_fence_before();
