@@ -41,29 +41,80 @@ UNIT = "nodes/s"
 UT_MAX_DEPTH = 24   # GDN_UT_MAX_DEPTH: deeper batches are verified by walking chains
 
 
-def measured_traffic():
-    """DRAM bytes per verify call from the committed ncu capture, if the kernels have not changed since."""
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "traffic_gdn_tree_verify_batched32x48.txt")
+# the files each measured kernel is built from: a record stays valid while their hashes do
+KERNEL_SOURCES = {
+    "ut_tcp_verify_kernel": ["gdn_verify_tcp.cu", "gdn_tile.cuh", "gdn_umma.cuh", "gdn_internal.h"],
+    "conv_window_kernel": ["gdn_conv.cu", "gdn_internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic_gdn_tree_verify_batched32x48.txt")
-    try:
-        fields = {}
-        for line in open(path):
-            if line.startswith("#") or not line.strip():
-                continue
-            parts = line.split()
-            fields[parts[0]] = parts[1]
-        csrc = os.path.join(ROOT, "gated_deltanet_tree_gb300", "csrc")
-        h = hashlib.sha256()
-        for f in sorted(os.listdir(csrc)):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
-        with open(os.path.join(ROOT, "include", "gdn_tree.h"), "rb") as fh:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "gated_deltanet_tree_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-        if h.hexdigest() != fields.get("source_sha256"):
-            return None
-        return float(fields["traffic_bytes_per_call"])
+    return h.hexdigest()
+
+
+def measured_traffic(units: int):
+    """DRAM bytes of one verify call over `units` (request, layer) blocks, from the committed small-case
+    capture of each kernel (bytes per block, scaled), or None once a kernel's sources changed since."""
+    try:
+        total = 0.0
+        seen = set()
+        for line in open(TRAFFIC_RECORD):
+            parts = line.split()
+            if not parts or parts[0] != "kernel":
+                continue
+            f = dict(zip(parts[2::2], parts[3::2]))
+            name = parts[1]
+            if f.get("sources_sha256") != kernel_source_hash(name):
+                return None
+            total += float(f["bytes_per_block"]) * units
+            seen.add(name)
+        return total if seen == set(KERNEL_SOURCES) else None
     except Exception:
         return None
+
+
+def record_traffic(csv_paths, blocks: int, command: str):
+    """Writes the traffic record from ncu CSV logs (dram__bytes_read.sum and dram__bytes_write.sum of the
+    captured launches of each kernel) of a capture over `blocks` (request, layer) blocks."""
+    import csv
+    import subprocess as sp
+    per = {}
+    for path in csv_paths:
+        with open(path) as fh:
+            rows = [r for r in csv.reader(l for l in fh if l.startswith('"'))]
+        hdr = rows[0]
+        ki, mi, vi, ii = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value"), hdr.index("ID")
+        for r in rows[1:]:
+            name = next((k for k in KERNEL_SOURCES if k in r[ki]), None)
+            if name is None or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                continue
+            per.setdefault(name, {}).setdefault(r[ii], {})[r[mi]] = float(r[vi].replace(",", ""))
+    commit = sp.run(["git", "-C", ROOT, "rev-parse", "--short=12", "HEAD"], capture_output=True, text=True).stdout.strip()
+    lines = ["# DRAM traffic of one gdn_tree_verify call per (request, layer) block, by kernel, from a capture over",
+             f"# {blocks} blocks (a small case whose state is larger than L2), scaled by bench.py to the call's blocks",
+             "# (traffic grows with the blocks: state, node rows and factors are per block; the conv weights, per",
+             "# layer, are the only exception, under 0.1% of a call).  Captured at commit " + (commit or "?") + ".",
+             "# Command (after the same bench command without ncu exited 0; one kernel per ncu call):",
+             f"#   {command}",
+             "# A kernel's line counts only while sources_sha256 equals the sha256 of its files (bench.py,",
+             "# KERNEL_SOURCES); otherwise roofline.traffic is reported as null."]
+    for name in KERNEL_SOURCES:
+        launches = list(per.get(name, {}).values())
+        if not launches:
+            raise SystemExit(f"no launches of {name} in {csv_paths}")
+        rd = statistics.mean(l["dram__bytes_read.sum"] for l in launches)
+        wr = statistics.mean(l["dram__bytes_write.sum"] for l in launches)
+        lines.append(f"kernel {name} sources_sha256 {kernel_source_hash(name)} bytes_per_block {(rd + wr) / blocks:.1f} "
+                     f"read_per_launch {rd:.0f} write_per_launch {wr:.0f} launches {len(launches)}")
+    with open(TRAFFIC_RECORD, "w") as fh:
+        fh.write("\n".join(lines) + "\n")
+    print("\n".join(lines))
 
 
 def tf32_peak() -> float:
@@ -138,7 +189,7 @@ def algorithmic_fma(w: S.Workload, n_per_req, updates_per_req, pend_len_per_req)
     return per_elem * w.layers * w.Hv * w.dk * w.dv
 
 
-TC_MAX_NODES = 32   # the tensor-core UT kernel takes d_v = 128 and n_max <= 32 (gdn_tree_verify's dispatch)
+TC_MAX_NODES = 32   # the tensor-core UT kernels take d_v = 128 and n_max <= 32 (gdn_tree_verify's dispatch)
 
 
 def tc_applies(w: S.Workload) -> bool:
@@ -146,13 +197,12 @@ def tc_applies(w: S.Workload) -> bool:
 
 
 def tc_mma_shapes(w: S.Workload, n: int):
-    """(M, N, K) of every tcgen05 MMA the tensor-core UT kernel issues for one head and a tree of n nodes
-    (NB = n rounded up to 8, NG = NB rounded up to 16; K = 8 per instruction, d_k / 8 instructions each):
-    the Gram rows (the operand's 128 rows times the high and times the low k rows), T0^T_hi times all
-    4 NB rows (high and low k, q), T0^T_lo times the 2 NB high rows."""
+    """(M, N, K) of every tcgen05 MMA the persistent tensor-core kernel issues for one head and a tree of n
+    nodes (NB = n rounded up to 8; K = 8 per instruction, d_k / 8 instructions each): T0^T_hi times all
+    4 NB operand rows (high and low k, q), then T0^T_lo times the 2 NB high rows.  (Its Gram coefficients
+    are formed on the CUDA cores, once per k-head.)"""
     nb = (n + 7) // 8 * 8
-    ng = (nb + 15) // 16 * 16
-    per_step = [(128, ng, 8), (128, ng, 8), (w.dv, 4 * nb, 8), (w.dv, 2 * nb, 8)]
+    per_step = [(w.dv, 4 * nb, 8), (w.dv, 2 * nb, 8)]
     return per_step * (w.dk // 8)
 
 
@@ -179,8 +229,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/gdn_clocks_{os.getpid()}.csv"
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"gdn_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -227,16 +277,16 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 
 def _oracle_unit(args):
-    cfg_kw, b, l = args
-    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    """Oracle verify of one (request, layer) block at one step: every node's root path replayed from the
+    block's initial state (the cost does not depend on the state's values, so no commit history is replayed)."""
+    cfg_kw, b, l, step = args
     sys.path.insert(0, ROOT)
     import synthetic as S2
     from oracle import gdn_oracle as O
     w = S2.Workload(**cfg_kw)
-    parent = S2.tree_for(w, b, 0)
+    parent = S2.tree_for(w, b, step)
     n = len(parent)
-    x, be, ag = S2.node_inputs(w, b, l, 0)
+    x, be, ag = S2.node_inputs(w, b, l, step)
     d = O.dims_of(w)
     T = S2.init_state(w, b, l).astype(np.float64)
     W = S2.init_conv_state(w, b, l).astype(np.float64)
@@ -254,46 +304,81 @@ def _warm_worker(_):
     return 0
 
 
-def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None, warmup: int = 0, steps: int = 0):
-    """Oracle verify (one full root-path replay per node) on a sample of (request, layer) blocks.
+def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None, warmup: int = 0, steps: int = 0,
+                      full: bool = False, all_steps: bool = False):
+    """The oracle (one full root-path replay per node, fp64) on `cores` host processes (spawn pool, one BLAS
+    thread each), on (request, layer) blocks of the workload.
 
-    With steps > 0: `warmup` untimed and `steps` timed steps, each one block per host process.
-    Otherwise: as many such steps as fit in about `target_s` seconds.
+    full: every block of step 0, once (the whole call).  Otherwise a seeded sample drawn from every block of
+    step 0 (or, with all_steps, of every step of the cycle): `warmup` untimed and `steps` timed rounds of
+    one block per process, or as many rounds as fit in about `target_s` seconds.
     """
     import dataclasses
     cores = cores or os.cpu_count() or 1
     kw = dataclasses.asdict(w)
-    units = [(kw, b, l) for l in range(w.layers) for b in range(w.B)]
-    order = np.random.default_rng(0).permutation(len(units))
+    nsteps = w.steps if all_steps else 1
+    units = [(kw, b, l, s) for s in range(nsteps) for l in range(w.layers) for b in range(w.B)]
+    order = np.random.default_rng(0).permutation(len(units)) if not full else np.arange(len(units))
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"   # inherited by the spawned workers
+    os.environ["OMP_NUM_THREADS"] = "1"
     ctx = mp.get_context("spawn")
     done_units, blocks, pos, timed_steps = 0, 0, 0, 0
 
     def next_batch():
         nonlocal pos
-        batch = [units[order[(pos + i) % len(units)]] for i in range(cores)]
-        pos += cores
+        take = min(cores, len(units) - pos) if full else cores
+        batch = [units[order[(pos + i) % len(units)]] for i in range(take)]
+        pos += take
         return batch
 
     with ctx.Pool(cores) as pool:
         pool.map(_warm_worker, range(cores))      # spawn and imports are not timed
         for _ in range(warmup):
             pool.map(_oracle_unit, next_batch())
+        if full:
+            pos = 0
         t0 = time.perf_counter()
         while True:
-            for u, _ in pool.map(_oracle_unit, next_batch()):
+            batch = next_batch()
+            for u, _ in pool.map(_oracle_unit, batch):
                 done_units += u
                 blocks += 1
             timed_steps += 1
-            if steps > 0 and timed_steps >= steps:
+            if full and pos >= len(units):
                 break
-            if steps <= 0 and time.perf_counter() - t0 >= target_s:
+            if not full and steps > 0 and timed_steps >= steps:
+                break
+            if not full and steps <= 0 and time.perf_counter() - t0 >= target_s:
                 break
     dt = time.perf_counter() - t0
+    total = w.B * w.layers * nsteps
+    what = (f"one whole verify call ({total} (request, layer) block{'s' if total > 1 else ''})" if full else
+            f"{blocks} of {total} (request, layer) blocks ({100.0 * blocks / total:.2f}%, seeded sample"
+            + (f" over all {nsteps} steps of the cycle" if all_steps else " of step 0") + ")")
     return {"value": done_units / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "steps": timed_steps,
-            "ms_per_step": dt * 1e3 / timed_steps,
-            "sample": f"{blocks} of {w.B * w.layers} (request, layer) blocks of step 0 ({timed_steps} steps of "
-                      f"{cores}), all {w.Hv} v-heads and every node, {dt:.1f} s wall on {cores} host processes "
-                      f"(spawn pool)"}
+            "ms_per_step": dt * 1e3 / timed_steps, "seconds": dt,
+            "sample": f"{what}, all {w.Hv} v-heads and every node, {dt:.2f} s wall on {cores} host "
+                      f"process{'es' if cores > 1 else ''} (spawn pool, one BLAS thread each)"}
+
+
+def cpu_baselines(w: S.Workload, seconds: float):
+    """The oracle on 1 thread and on all host cores: configs 1-3 in full (one verify call each), and a sample
+    of the headline workload across its whole cycle.  Run before the first GPU call of the process."""
+    ncores = os.cpu_count() or 1
+    main_all = oracle_throughput(w, target_s=seconds, cores=ncores, all_steps=True)
+    main_one = oracle_throughput(w, target_s=seconds * 0.6, cores=1, all_steps=True)
+    per = {}
+    for cfg in (1, 2, 3):
+        wc = S.workload(cfg)
+        one = oracle_throughput(wc, cores=1, full=True)
+        allc = oracle_throughput(wc, cores=ncores, full=True)
+        per[str(cfg)] = {"workload": wc.name, "one_thread": {k: one[k] for k in ("value", "seconds", "sample")},
+                         "all_cores": {k: allc[k] for k in ("value", "seconds", "sample", "cores")}}
+    out = dict(main_all)
+    out["nproc"] = ncores
+    out["one_thread"] = {k: main_one[k] for k in ("value", "seconds", "sample", "cores")}
+    out["per_config"] = per
+    return out
 
 
 def reduce_across_ranks(ms: float, units: float, e2e_ms: float, e2e_units: float, device=None):
@@ -436,8 +521,9 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
 
     # end to end through the public API with host buffers: inputs H2D from pinned memory, outputs D2H
     # A/B: the same steps with per-node-state schedules (every node reloads its parent's stored state)
-    ab = walk = simt = tc1 = None
+    ab = walk = simt = tc1 = bout = None
     if not args.no_ab:
+        bout = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="boundary_out")
         if tc_applies(w) and not any(walks[args.warmup:]):
             tc1 = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="tc_per_head")
             simt = run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode="ut_simt")
@@ -461,7 +547,7 @@ def run_gpu(args, w: S.Workload, rank: int, world: int):
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
                                 (clk or {}).get("sm_max_mhz") or 2070.0)
     return dict(ms=ms, units=timed_units_all, verify_ms=verify_ms, finish_ms=finish_ms, clocks=clk, ab=ab, walk=walk,
-                simt=simt, tc1=tc1, avg_tflops=avg_tflops,
+                simt=simt, tc1=tc1, bout=bout, avg_tflops=avg_tflops,
                 achieved=achieved, peak=peak, peak_kind=peak_kind, avg_bytes=avg_bytes, e2e_ms=e2e_ms,
                 avg_flops=avg_flops, alu_peak=alu_peak, avg_verify_s=avg_verify_s,
                 e2e_units=e2e_units_all, e2e=e2e, nb_cap=gs.nb_cap, walked=any(walks[args.warmup:]),
@@ -484,8 +570,11 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode):
         packed.append(torch.from_numpy(words).to(dev))
         nb_cap = max(nb_cap, nb)
         depth.append(dm)
-    flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | {"ut_simt": N.GDN_VERIFY_UT_SIMT, "tc_per_head": N.GDN_VERIFY_TC_PER_HEAD}.get(
-        mode, N.GDN_VERIFY_CHAIN_WALK)
+    if mode == "boundary_out":   # the default kernel, every boundary state stored (the ABI's default)
+        flags = 0
+    else:
+        flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | {"ut_simt": N.GDN_VERIFY_UT_SIMT,
+                                                 "tc_per_head": N.GDN_VERIFY_TC_PER_HEAD}.get(mode, N.GDN_VERIFY_CHAIN_WALK)
     boundary = torch.empty(w.B, w.layers, nb_cap, w.Hv, w.dk, w.dv, dtype=torch.float32, device=dev)
     ver = gs.ver
 
@@ -515,7 +604,8 @@ def run_walk_ab(args, w, gs, dev, stream, paths, parents_host, mode):
     return {"schedule": {"per_node": "per-node states in HBM (no heavy edges)",
                          "walk": "heavy-light chain walk, branch states in tensor memory",
                          "ut_simt": "tree-masked UT form on the CUDA cores (ut_verify_kernel)",
-                         "tc_per_head": "tree-masked UT form on the tensor cores, a CTA per v-head (ut_tc_verify_kernel)"}[mode],
+                         "tc_per_head": "tree-masked UT form on the tensor cores, a CTA per v-head (ut_tc_verify_kernel)",
+                         "boundary_out": "default kernel with every boundary state stored to HBM (flags 0)"}[mode],
             "steps": steps, "nb_max": nb_cap,
             "ms_per_step": ms / steps, "value": units / (ms / 1e3), "unit": UNIT}
 
@@ -600,6 +690,122 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
     return dict(ms=ms, units=units, steps=steps, h2d=h2d, d2h=d2h)
 
 
+def device_inputs(w: S.Workload, dev, seed: int):
+    """Seeded inputs generated on the device with the workload's value recipe (host generation of the
+    128-request configurations would take minutes): x ~ N(0, 1), beta = sigmoid(N(0, 1)) and
+    log g = -softplus(N(0, 1)) in the input dtype; returns (x, beta, log_g)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if w.in_dtype == S.DTYPE_BF16 else torch.float32
+    sh = (w.B, w.layers, w.n_max)
+    x = torch.randn(*sh, w.C, generator=g, device=dev).to(dt)
+    be = torch.sigmoid(torch.randn(*sh, w.Hv, generator=g, device=dev)).to(dt)
+    ag = (-torch.nn.functional.softplus(torch.randn(*sh, w.Hv, generator=g, device=dev))).to(dt)
+    return x, be, ag
+
+
+def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
+    """One bench line per further configuration: the verify -> commit loop on seeded synthetic inputs of that
+    configuration's shapes (trees and accepted paths from the host generators, activations and states
+    generated on the device), boundary states as scratch, CUDA events around every verify call."""
+    import torch
+    from gated_deltanet_tree_gb300 import _native as N
+    from gated_deltanet_tree_gb300.runtime import TreeVerifier, paths_tensor
+    from harness import dims_for
+    w = S.workload(cfg)
+    dims = dims_for(w)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + cfg)
+    f32 = dict(dtype=torch.float32, device=dev)
+    state = torch.randn(w.B, w.layers, w.Hv, w.dk, w.dv, generator=g, **f32).mul_(0.1)
+    conv_state = torch.randn(w.B, w.layers, max(w.K - 1, 0), w.C, generator=g, **f32)
+    conv_w = torch.randn(w.layers, w.C, w.K, generator=g, **f32).mul_(1.0 / math.sqrt(w.K))
+    out_o = torch.empty(w.B, w.layers, w.n_max, w.Hv, w.dv, **f32)
+    ver = TreeVerifier(dims, w.B, w.layers, w.n_max, dev)
+    inputs = [device_inputs(w, dev, 77 * cfg + i) for i in range(2)]   # two activation sets, alternated
+    trees = [[S.tree_for(w, b, s) for b in range(w.B)] for s in range(w.steps)]
+    paths = [[S.path_for(w, trees[s][b], b, s) for b in range(w.B)] for s in range(w.steps)]
+    words, depth, nreq = [], [], []
+    for s in range(w.steps):
+        P = np.full((w.B, w.n_max), -1, dtype=np.int32)
+        n = np.zeros(w.B, dtype=np.int32)
+        for b, p in enumerate(trees[s]):
+            P[b, :len(p)] = p
+            n[b] = len(p)
+        wd, _, dm = N.gdn_pack_schedules(P, n, with_depth=True)
+        words.append(torch.from_numpy(wd).to(dev))
+        depth.append(dm)
+        nreq.append([len(p) for p in trees[s]])
+    pt = [paths_tensor(paths[s], w.n_max, dev) for s in range(w.steps)]
+    # the tree-masked UT kernels store no state but the committed one with boundary states as scratch, and a
+    # pure chain stashes nothing, so no boundary buffer is needed (nb_max = 0)
+    dummy = torch.empty(16, **f32)
+
+    def one(i, ev=None):
+        s = i % w.steps
+        X, BE, AG = inputs[i % 2]
+        sc = N.gdn_batch_schedule(B=w.B, n_max=w.n_max, nb_max=0, depth_max=depth[s], words=words[s].data_ptr())
+        if ev is not None:
+            ev[0].record()
+        N.gdn_tree_verify(dims, w.layers, sc, X, conv_w, BE, AG, state, conv_state, out_o, dummy, ver.banks,
+                          ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, None)
+        if ev is not None:
+            ev[1].record()
+        N.gdn_commit_fold(dims, w.layers, sc, pt[s][0], pt[s][1], 0, ver.banks, None)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize(dev)
+    ver.check_error()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(steps):
+        one(warmup + k, evs[k])
+    t1.record()
+    torch.cuda.synchronize(dev)
+    ver.check_error()
+    ms = t0.elapsed_time(t1)
+    vms = [a.elapsed_time(b) for a, b in evs]
+    units = sum(sum(nreq[(warmup + k) % w.steps]) for k in range(steps)) * w.layers * w.Hv
+    byts, fmas, walked = [], [], False
+    for k in range(steps):
+        i = warmup + k
+        s = i % w.steps
+        prev = paths[(i - 1) % w.steps]
+        L = [len(p) for p in prev]
+        byts.append(algorithmic_bytes(w, nreq[s], [0] * w.B, L))
+        walk = depth[s] > UT_MAX_DEPTH
+        walked = walked or walk
+        ups = ([int((np.bincount(p[1:], minlength=len(p)) > 0).sum()) if len(p) > 1 else 0 for p in trees[s]]
+               if walk else [0] * w.B)
+        fmas.append(algorithmic_fma(w, nreq[s] if (walk or not tc_applies(w)) else [0] * w.B, ups, L))
+    peak, peak_kind = peaks()
+    avg_v = statistics.mean(vms) / 1e3
+    alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count, 2070.0)
+    gbs = statistics.mean(byts) / avg_v / 1e9
+    tf = 2 * statistics.mean(fmas) / avg_v / 1e12
+    kernel = ("chain_verify_kernel (heavy-light chain walk: depth > %d)" % UT_MAX_DEPTH if walked else
+              "ut_tcp_verify_kernel (tensor cores, persistent)" if tc_applies(w) else
+              "ut_verify_kernel (tree-masked UT form, CUDA cores)")
+    line = {"workload": w.name, "requests": w.B, "gdn_layers": w.layers, "tree": f"{w.budget}-node {w.tree}",
+            "value": units / (ms / 1e3), "unit": UNIT, "steps": steps, "warmup": warmup,
+            "ms_per_step": ms / steps, "verify_ms_per_call": statistics.mean(vms),
+            "us_per_call": 1e3 * statistics.mean(vms), "kernel": kernel + " + conv_window_kernel",
+            "algorithmic_bytes_per_call": statistics.mean(byts),
+            "hbm": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_kind": peak_kind},
+            "alu": {"achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                    "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x 2070 MHz",
+                    "algorithmic_flops_per_call": 2 * statistics.mean(fmas)},
+            "bound": "alu" if tf / alu_peak > gbs / peak else "hbm",
+            "inputs": "trees and paths from the host generators; activations, states and conv weights seeded on "
+                      "the device with the same distributions; two activation sets alternate"}
+    del state, conv_state, conv_w, out_o, ver, inputs, words, pt
+    torch.cuda.empty_cache()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -613,12 +819,20 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override GDN layers (smaller profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ab", action="store_true", help="skip the per-node-state A/B run")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the lines of configurations 2, 3, 5(i), 5(ii)")
+    ap.add_argument("--record-traffic", nargs="+", default=None, metavar="CSV",
+                    help="write the traffic record from ncu CSV logs of a capture (with --requests, --layers "
+                         "giving its blocks and --traffic-command the command) and exit")
+    ap.add_argument("--traffic-command", default="")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = S.workload(args.workload)
+    if args.record_traffic:
+        record_traffic(args.record_traffic, (args.requests or w.B) * (args.layers or w.layers), args.traffic_command)
+        return
     if args.requests:
         w = w.replace(B=args.requests)
     if args.layers:
@@ -627,7 +841,10 @@ def main():
               "dk": w.dk, "dv": w.dv, "conv_K": w.K, "tree": f"{w.budget}-node top-{w.top_k} DDTree" if
               w.tree == "ddtree" else f"{w.budget}-node {w.tree}", "steps_cycle": w.steps,
               "l2": "inputs larger than L2 (state alone is %.1f GB)" % (w.B * w.layers * w.Hv * w.dk * w.dv * 4 / 1e9),
-              "parallelism": f"replicas x{args.gpus}"}
+              "parallelism": f"replicas x{args.gpus}",
+              "boundary_states": "scratch (GDN_VERIFY_BOUNDARY_SCRATCH): the tree-masked UT form forms no boundary "
+                                 "state, so none is stored; ab_boundary_output times the same steps with every "
+                                 "boundary state stored to HBM (the call's default)"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -657,10 +874,18 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # the spawn pool starts before the first GPU call of this process
-        cpu = oracle_throughput(w, target_s=args.cpu_seconds)
+        # the spawn pools start before the first GPU call of this process
+        cpu = cpu_baselines(w, args.cpu_seconds)
 
     r = run_gpu(args, w, rank, world)
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config and args.workload == 4 and not args.requests:
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        per_config = {}
+        for cfg, key in ((2, "2_qwen_layer_B1"), (3, "3_48_layers_B1"), (5, "5i_128x48_ddtree64_top8"),
+                         (6, "5ii_128x48_chain64")):
+            per_config[key] = run_config(cfg, dev, steps=8 if cfg <= 3 else 4, warmup=3 if cfg <= 3 else 2)
     if rank != 0:
         return
     value = r["units"] / (r["ms"] / 1e3)
@@ -679,7 +904,10 @@ def main():
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
                      "avg_launch_ms": statistics.mean(r["verify_ms"]),
-                     "traffic": measured_traffic() if w.cfg == 4 and w.B == 32 and w.layers == 48 else None,
+                     "traffic": measured_traffic(w.B * w.layers),
+                     "traffic_note": "DRAM bytes of the whole call (both kernels) per launch, scaled from the committed "
+                                     "small-case capture (profiles/traffic_gdn_tree_verify_batched32x48.txt); null once a "
+                                     "kernel changed since",
                      "alu": {"achieved": r["avg_flops"] / r["avg_verify_s"] / 1e12, "peak": r["alu_peak"],
                              "unit": "TFLOP/s", "frac": r["avg_flops"] / r["avg_verify_s"] / 1e12 / r["alu_peak"],
                              "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x max SM clock",
@@ -697,6 +925,8 @@ def main():
             "host_per_step": ("DDTree construction from the draft tables, " if w.tree == "ddtree" else "")
                              + "heavy-light schedules, packing"},
         "gpu_launches": r["gpu_launches"],
+        "ab_boundary_output": None if r["bout"] is None else dict(
+            r["bout"], cost_vs_scratch=r["bout"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_tc_per_head": None if r["tc1"] is None else dict(
             r["tc1"], persistent_speedup=r["tc1"]["ms_per_step"] / (r["ms"] / args.steps)),
         "ab_ut_simt": None if r["simt"] is None else dict(
@@ -706,6 +936,7 @@ def main():
         "ab_per_node_states": None if r["ab"] is None else dict(
             r["ab"], hld_speedup=r["ab"]["ms_per_step"] / r["walk"]["ms_per_step"],
             ut_speedup=r["ab"]["ms_per_step"] / (r["ms"] / args.steps)),
+        "per_config": per_config,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -93,13 +93,33 @@ def test_hbm_stashes_counts_spilled_pushes():
 
 
 def test_tensor_core_flops_follow_the_issued_mmas():
-    """One head, one layer: the tf32 FLOPs reported are those of the MMAs the kernel issues (two Gram
-    MMAs, one N = 4 NB and one N = 2 NB product per K step of 8), and the kernel applies where the
-    dispatch sends batches to it."""
+    """One head, one layer: the tf32 FLOPs reported are those of the MMAs the persistent kernel issues (one
+    N = 4 NB and one N = 2 NB product per K step of 8), and the kernel applies where the dispatch sends
+    batches to it."""
     import bench
     w = S.workload(2).replace(Hk=1, Hv=1, layers=1, B=1)
     shapes = bench.tc_mma_shapes(w, 22)
-    assert len(shapes) == 4 * 128 // 8
-    assert sorted({n for _, n, _ in shapes}) == [32, 48, 96]   # NG, 2 NB, 4 NB for NB = 24
-    assert bench.tensor_flops(w, [22]) == 16 * 2 * 128 * 8 * (32 + 32 + 96 + 48)
+    assert len(shapes) == 2 * 128 // 8
+    assert sorted({n for _, n, _ in shapes}) == [48, 96]   # 2 NB, 4 NB for NB = 24
+    assert bench.tensor_flops(w, [22]) == 16 * 2 * 128 * 8 * (96 + 48)
     assert bench.tc_applies(w) and not bench.tc_applies(w.replace(n_max=64)) and not bench.tc_applies(w.replace(dv=64))
+
+
+def test_traffic_record_roundtrip(tmp_path, monkeypatch):
+    """The traffic record written from ncu CSV logs scales per (request, layer) block and is dropped as soon
+    as one measured kernel's sources differ from those the capture was taken with."""
+    import bench
+    csv = tmp_path / "t.csv"
+    hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",' \
+          '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n'
+    rows = []
+    for i, (k, rd, wr) in enumerate([("ut_tcp_verify_kernel<128, bf16, 2>", 900, 700), ("conv_window_kernel<bf16, 4>", 300, 100)]):
+        for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr)):
+            rows.append(f'"{i}","1","p","h","{k}","1","7","(1,1,1)","(1,1,1)","0","10.3","s","{m}","byte","{v:,}"\n')
+    csv.write_text("==PROF== noise\n" + hdr + "".join(rows))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(tmp_path / "rec.txt"))
+    bench.record_traffic([str(csv)], blocks=4, command="ncu ...")
+    assert bench.measured_traffic(8) == (1600 + 400) / 4 * 8
+    src = dict(bench.KERNEL_SOURCES)
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", dict(src, conv_window_kernel=["gdn_commit.cu"]))
+    assert bench.measured_traffic(8) is None
