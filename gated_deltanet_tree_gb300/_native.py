@@ -35,6 +35,7 @@ GDN_VERIFY_BOUNDARY_SCRATCH = 1
 GDN_VERIFY_CHAIN_WALK = 2
 GDN_VERIFY_UT_SIMT = 4
 GDN_VERIFY_TC_PER_HEAD = 8
+GDN_VERIFY_CHAINS = 16
 GDN_MAX_NODES = 64
 
 

@@ -149,7 +149,8 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
                            float* conv_state, float* out_o, float* boundary_states, gdn_banks* banks,
                            void* workspace, size_t workspace_bytes, int32_t flags, cudaStream_t stream) {
   gdn::clear_error();
-  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD))
+  if (flags & ~(GDN_VERIFY_BOUNDARY_SCRATCH | GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD |
+                GDN_VERIFY_CHAINS))
     return fail(GDN_ERR_INVALID_ARG, "unknown verify flags 0x%x", flags);
   GDN_TRY(check_dims(d));
   GDN_TRY(check_sched(sched));
@@ -198,19 +199,25 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   vp.u_out = banks->u[cur]; vp.a_out = banks->a[cur];
   vp.state = state; vp.out_o = out_o; vp.boundary = boundary_states;
   vp.boundary_out = (flags & GDN_VERIFY_BOUNDARY_SCRATCH) ? 0 : 1;
-  // the UT form costs depth^2 per node and depth per (node, column): deep trees walk their chains
-  vp.chain_walk = ((flags & GDN_VERIFY_CHAIN_WALK) || sched->depth_max > GDN_UT_MAX_DEPTH) ? 1 : 0;
+  // the UT form costs depth^2 per node and depth per (node, column): deep trees walk their chains, unless
+  // the caller says every tree is a chain, which the tensor cores then solve in 16-node segments
+  const bool chains_tc = (flags & GDN_VERIFY_CHAINS) && !(flags & (GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT)) &&
+                         gdn::verify_tcp_supported(d->dk, d->dv, n_max, true);
+  vp.chain_walk = !chains_tc && ((flags & GDN_VERIFY_CHAIN_WALK) || sched->depth_max > GDN_UT_MAX_DEPTH) ? 1 : 0;
   vp.fold = pend >= 0;
   if (pend >= 0) {
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];
   }
   vp.pend_path = banks->pend_path; vp.pend_len = banks->pend_len; vp.err = banks->err;
-  if (vp.chain_walk) {
+  if (chains_tc) {
+    e = gdn::launch_verify_tcp(vp, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, chain segments)");
+  } else if (vp.chain_walk) {
     e = gdn::launch_verify(vp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "chain-verify launch");
   } else if (!(flags & (GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD)) &&
-             gdn::verify_tcp_supported(d->dk, d->dv, n_max)) {
-    e = gdn::launch_verify_tcp(vp, stream);
+             gdn::verify_tcp_supported(d->dk, d->dv, n_max, false)) {
+    e = gdn::launch_verify_tcp(vp, false, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, persistent)");
   } else if (!(flags & GDN_VERIFY_UT_SIMT) && gdn::verify_tc_supported(d->dk, d->dv, n_max)) {
     e = gdn::launch_verify_tc(vp, stream);

@@ -152,8 +152,9 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);      // chain 
 cudaError_t launch_verify_ut(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, CUDA cores
 cudaError_t launch_verify_tc(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, tensor cores, a CTA per head
 bool verify_tc_supported(int dk, int dv, int n_max);
-cudaError_t launch_verify_tcp(const VerifyParams& p, cudaStream_t s);  // the same, persistent and warp-specialised
-bool verify_tcp_supported(int dk, int dv, int n_max);
+// the same, persistent and warp-specialised; chain: every tree is a pure chain, solved in 16-node segments
+cudaError_t launch_verify_tcp(const VerifyParams& p, bool chain, cudaStream_t s);
+bool verify_tcp_supported(int dk, int dv, int n_max, bool chain);
 
 cudaError_t launch_commit(const CommitParams& p, int compact, cudaStream_t s);
 bool verify_supported(int dk, int dv);

@@ -59,6 +59,8 @@ constexpr int kPDv = 128;          // d_v: the MMA's M and the threads of a grou
 constexpr int kPGroup = 128;       // threads per compute group
 constexpr int kPFold = 8;          // pending rows staged per fold chunk
 constexpr int kPMaxNodes = 32;     // 4 NB <= 128 D columns
+constexpr int kPSeg = 16;          // chain mode: nodes per segment
+constexpr int kPMaxChain = 64;     // chain mode: longest chain
 
 // ---- small PTX helpers
 // One non-blocking test of phase `parity` of `bar`.
@@ -132,19 +134,25 @@ __device__ __forceinline__ float tmem_ld1(uint32_t ta) {
   return v;
 }
 
-// Shared-memory layout in bytes: NG group regions, then the CTA's barriers and words.
+// Shared-memory layout in bytes: NG group regions, then the CTA's barriers and words.  `seg` is the most
+// nodes solved at once (the whole tree, or a chain segment): the operand, the depth stack and a segment's
+// pairs are sized by it; rows and per-node tables by n_max.
 struct PLayout {
-  int n_max, dk;
+  int n_max, dk, seg;
   __host__ __device__ static int a16(int x) { return (x + 15) & ~15; }
-  __host__ __device__ int nbm() const { return (n_max + 7) & ~7; }
-  __host__ __device__ int pairs() const { return n_max * (n_max - 1) / 2; }
+  __host__ __device__ int nbm() const { return (seg + 7) & ~7; }
+  // ancestor pairs inside segments, over all segments of an n_max-node tree or chain
+  __host__ __device__ int pairs() const {
+    const int full = n_max / seg, r = n_max % seg;
+    return full * (seg * (seg - 1) / 2) + r * (r - 1) / 2;
+  }
   __host__ __device__ int words() const { return 5 + 4 * n_max; }
   // one group's region
   __host__ __device__ int opnd() const { return 0; }                                 // [dk/4][4 NB][16 B] operand
   __host__ __device__ int stg() const { return opnd() + 4 * nbm() * dk * 4; }         // [2][n_max][dk] k, q rows
   __host__ __device__ int vbuf() const { return stg() + 2 * n_max * dk * 4; }         // [n_max][128] v, then u
-  __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [n_max][128] u by depth
-  __host__ __device__ int pk() const { return stk() + n_max * kPDv * 4; }             // [kPFold][dk] pending k
+  __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [seg][128] u by depth
+  __host__ __device__ int pk() const { return stk() + seg * kPDv * 4; }               // [kPFold][dk] pending k
   __host__ __device__ int pu() const { return pk() + kPFold * dk * 4; }               // [kPFold][128] pending u
   __host__ __device__ int ptab() const { return pu() + kPFold * kPDv * 4; }           // [pairs] (A, C, s dv, -)
   __host__ __device__ int hsc() const { return ptab() + a16(pairs() * 16); }          // [n_max] (g, beta, bG, G)
@@ -164,13 +172,17 @@ struct PLayout {
   __host__ __device__ int bytes(int ng) const { return shared(ng) + ng * 4 * 8 + 16; }
 };
 
-template <int DK, typename InT, int NG>
+// CHAIN: every tree is a pure chain (parent[i] = i - 1), solved in segments of kPSeg nodes: each segment is
+// a chain in the UT form from the running state, which then absorbs the segment by the fold's operations
+// (the chunked UT form of a long chain); otherwise the whole tree is one segment (n_max <= 32).
+template <int DK, typename InT, int NG, bool CHAIN>
 __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyParams p, int n_items, int hpi) {
   constexpr int DV = kPDv;
   constexpr int KC = DK / 4;                    // 16-byte chunks of a k or q row
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char smem[];
-  const PLayout L{p.n_max, DK};
+  const PLayout L{p.n_max, DK, CHAIN ? kPSeg : p.n_max};
+  const int SEG = CHAIN ? kPSeg : p.n_max;      // nodes per segment
   const int n_max = p.n_max;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -335,6 +347,36 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       return p.state + (static_cast<size_t>(x.bl) * p.Hv + h) * DK * DV + c;
     };
 
+    // the [k | q] operand of nodes s0 .. s0 + ns from the staged rows: tf32 high rows r < 2 NB and low rows
+    // 2 NB + r (NB = ns rounded up to 8, rows past ns zero); a warp step covers 8 rows x 4 chunks with the
+    // chunk index rotated by the row, so reads and writes each hit distinct banks
+    auto build_operand = [&](int s0, int ns, int NB) {
+      const int kbn = (KC + 7) / 8;
+      const int steps = (2 * NB / 8) * kbn * 2;
+      const int e = lane & 7, qd = lane >> 3;
+      for (int s = wq; s < steps; s += 4) {
+        const int rb8 = s / (2 * kbn), kb = (s >> 1) % kbn, hh = s & 1;
+        const int r = 8 * rb8 + e;
+        const int kc = 8 * kb + ((e + qd + 4 * hh) & 7);
+        if (kc < KC) {
+          const bool isq = r >= NB;
+          const int node = isq ? r - NB : r;
+          float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (node < ns) x4 = *reinterpret_cast<const float4*>(stg + ((isq ? n_max : 0) + s0 + node) * DK + 4 * kc);
+          float4 hi, lo;
+          hi.x = tf32_hi(x4.x); lo.x = tf32_lo(x4.x);
+          hi.y = tf32_hi(x4.y); lo.y = tf32_lo(x4.y);
+          hi.z = tf32_hi(x4.z); lo.z = tf32_lo(x4.z);
+          hi.w = tf32_hi(x4.w); lo.w = tf32_lo(x4.w);
+          *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
+          *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+        }
+      }
+      fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
+    };
+    // parent inside the node's segment (-1 at a segment's first node)
+    auto spar = [&](int v) { return CHAIN ? (v % kPSeg ? v - 1 : -1) : rec[lay.parent() + v]; };
+
     int k = g;
     Item cur = item_at(k);
     if (cur.it < n_items) {
@@ -362,41 +404,33 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       group_sync(gid);
       const int n = rec[0];
       bool item_ok = n >= 1 && n <= n_max && Lraw >= 0;
-      if (item_ok && c < n) item_ok = c == 0 ? parent[0] == -1 : (parent[c] >= 0 && parent[c] < c);
+      if (item_ok && c < n)
+        item_ok = c == 0 ? parent[0] == -1 : (CHAIN ? parent[c] == c - 1 : (parent[c] >= 0 && parent[c] < c));
       item_ok = group_and(gid, item_ok);
       if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
       ok = group_and(gid, mbar_wait_ab(b_kq, ph_kq, abortw));
       if (!ok) break;   // (still armed: the drain below waits for the copy)
       ph_kq ^= 1;
       armed_kq = false;
-      const int NB = (n + 7) & ~7;
+      const int NB = (n + 7) & ~7;   // (tree mode: the whole tree is one segment)
       if (item_ok) {
-        // [k | q] operand, tf32 high rows r < 2 NB and low rows 2 NB + r; a warp step covers 8 rows x 4
-        // chunks with the chunk index rotated by the row, so reads and writes each hit distinct banks
-        const int kbn = (KC + 7) / 8;
-        const int steps = (2 * NB / 8) * kbn * 2;
-        const int e = lane & 7, qd = lane >> 3;
-        for (int s = wq; s < steps; s += 4) {
-          const int rb8 = s / (2 * kbn), kb = (s >> 1) % kbn, hh = s & 1;
-          const int r = 8 * rb8 + e;
-          const int kc = 8 * kb + ((e + qd + 4 * hh) & 7);
-          if (kc < KC) {
-            const bool isq = r >= NB;
-            const int node = isq ? r - NB : r;
-            float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (node < n) x4 = *reinterpret_cast<const float4*>(stg + ((isq ? n_max : 0) + node) * DK + 4 * kc);
-            float4 hi, lo;
-            hi.x = tf32_hi(x4.x); lo.x = tf32_lo(x4.x);
-            hi.y = tf32_hi(x4.y); lo.y = tf32_lo(x4.y);
-            hi.z = tf32_hi(x4.z); lo.z = tf32_lo(x4.z);
-            hi.w = tf32_hi(x4.w); lo.w = tf32_lo(x4.w);
-            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
-            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+        if (!CHAIN) build_operand(0, n, NB);
+        // depths and pair offsets (warp 0, a lane per node), then every node's ancestors; in chain mode the
+        // depth inside a segment and the offsets have closed forms
+        if (CHAIN) {
+          constexpr int sp = kPSeg * (kPSeg - 1) / 2;
+          for (int t = c; t < n; t += kPGroup) {
+            const int dl = t % kPSeg;
+            const int o = (t / kPSeg) * sp + dl * (dl - 1) / 2;
+            dep[t] = dl;
+            coff[t] = o;
+            for (int m = 1; m <= dl; ++m) {
+              ranc[o + m - 1] = t - m;
+              ptn[o + m - 1] = t;
+            }
           }
-        }
-        fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
-        // depths and pair offsets (warp 0, a lane per node), then every node's ancestors
-        if (wq == 0) {
+          if (c == 0) coff[n] = (n / kPSeg) * sp + (n % kPSeg) * (n % kPSeg - 1) / 2;
+        } else if (wq == 0) {
           int d = 0;
           if (lane < n)
             for (int v = lane; v > 0; v = parent[v]) ++d;
@@ -425,7 +459,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       // node once, the root first, the depth rising by at most one per step, and each node's parent the last
       // node visited one level up (so the stack always holds the current node's root path).
       int wpack = 0;
-      if (item_ok) {
+      if (!CHAIN && item_ok) {
         const int w = lane;
         const int t = w < n ? (rec[lay.ops() + w] & kOpNode) : 0;
         const bool in = w < n && t < n;
@@ -479,10 +513,11 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       }
       fence_proxy_async();   // staging reads done before the next item's copies overwrite it
       group_sync(gid);
-      // the next item of this group: its k and q rows, record and path
+      // the next item of this group: its record and path, and its k and q rows (in chain mode the staged rows
+      // serve every segment of every head, so those follow after the item's last head)
       Item nxt = item_at(k + NG);
       if (nxt.it < n_items) {
-        issue_kq(nxt);
+        if (!CHAIN) issue_kq(nxt);
         load_item_regs(nxt);
       }
 
@@ -538,6 +573,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           issue_pend(nxi, nxh, min(kPFold, nx_lp), pe);
         }
 
+        if constexpr (!CHAIN) {
         // ---- 2. A = T0^T, high part, and its product with all 4 NB operand rows
         if (item_ok) {
 #pragma unroll
@@ -680,6 +716,182 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           }
         }
         tmem_fence_before();
+        } else {
+        // ---- 2 - 5 per segment: the whole tree, or the chain's segments of kPSeg nodes from the running state
+        for (int s0 = 0; s0 < n && ok; s0 += SEG) {
+          const int ns = CHAIN ? min(SEG, n - s0) : n, NBs = (ns + 7) & ~7;
+          const bool first = !CHAIN || s0 == 0, last = !CHAIN || s0 + SEG >= n;   // (tree mode: one segment)
+          if (CHAIN && item_ok) {   // this segment's operand (the previous segment's products have completed)
+            build_operand(s0, ns, NBs);
+            group_sync(gid);
+          }
+          // ---- 2. A = T0^T, high part, and its product with all 4 NB operand rows
+          if (item_ok) {
+#pragma unroll
+            for (int q = 0; q < DK / 16; ++q) {
+              float v[16];
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const float2 e2 = unpack2(R.T[8 * q + jj]);
+                v[2 * jj] = tf32_hi(e2.x);
+                v[2 * jj + 1] = tf32_hi(e2.y);
+              }
+              tmem_st16(tA + 16u * q, v);
+            }
+            tmem_wait_st();
+          }
+          tmem_fence_before();
+          group_sync(gid);
+          if (item_ok) {
+            if (c == 0) {
+              tmem_fence_after();
+              issue_mma(true, NBs);
+            }
+            armed_mma = true;
+          }
+          if (first && item_ok && Lp > 0) R.store(st, DV);   // the committed state, written once, while the product runs
+
+          // ---- 3. this head's coefficients, every segment at once: a thread of warps 1-2 per node walks its
+          // ancestors inside its segment (rho by products, no division), A_ts = beta_t rho_ts G_ts and
+          // C_ts = rho_ts H_ts into the pair table, Gamma_t from the segment's first node
+          if (first && item_ok && c >= 32 && c - 32 < n) {
+            const int t = c - 32;
+            const float4 sc = hsc[t];
+            float prod = 1.f;
+            int v = t, i = coff[t];
+            while (spar(v) >= 0) {
+              prod *= hsc[v].x;
+              v = spar(v);
+              const float2 q2 = gh[i];
+              ptab[i] = make_float4(sc.y * prod * q2.x, prod * q2.y, __int_as_float(v * DV), 0.f);
+              ++i;
+            }
+            const float gam_t = prod * hsc[v].x;
+            reinterpret_cast<float*>(hsc + t)[2] = sc.y * gam_t;
+            reinterpret_cast<float*>(hsc + t)[3] = gam_t;
+          }
+
+          // ---- the low part of A once the high product has read it, and its product with the high rows
+          if (item_ok) {
+            ok = group_and(gid, mbar_wait_ab(b_mma, ph_mma, abortw));
+            if (!ok) break;
+            ph_mma ^= 1;
+            armed_mma = false;
+            tmem_fence_after();
+#pragma unroll
+            for (int q = 0; q < DK / 16; ++q) {
+              float v[16];
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const float2 e2 = unpack2(R.T[8 * q + jj]);
+                v[2 * jj] = tf32_lo(e2.x);
+                v[2 * jj + 1] = tf32_lo(e2.y);
+              }
+              tmem_st16(tA + 16u * q, v);
+            }
+            tmem_wait_st();
+            tmem_fence_before();
+            group_sync(gid);   // also publishes the pair table and Gamma
+            if (c == 0) {
+              tmem_fence_after();
+              issue_mma(false, NBs);
+            }
+            armed_mma = true;
+          }
+
+          // ---- 4. after the last segment the registers are free: the next head's state column and gates
+          // (after the boundary replay instead, when boundary states are stored, since it replays from T0 in
+          // these registers)
+          if (last && !p.boundary_out && has_nx) {
+            R.load(state_ptr(nxi, nxh), DV);
+            load_head_regs(nxi, nxh, nx_lp, nx_same ? pth_cur : pth_nx);
+          }
+
+          // ---- 5. epilogue: forward substitution down the segment's nodes, column c
+          if (first) {
+            ok = group_and(gid, mbar_wait_ab(b_rows, ph_rows, abortw));
+            if (!ok) break;
+            ph_rows ^= 1;
+            armed_rows = false;
+          }
+          if (item_ok) {
+            ok = group_and(gid, mbar_wait_ab(b_mma, ph_mma, abortw));
+            if (!ok) break;
+            ph_mma ^= 1;
+            armed_mma = false;
+            tmem_fence_after();
+            const size_t ostride = static_cast<size_t>(p.Hv) * DV;
+            float* o_col = p.out_o + (nrow0 * p.Hv + h) * DV + c;
+            float* u_col = p.u_out + (nrow0 * p.Hv + h) * DV + c;
+            float* vcol = vbuf + c;
+            // one walk position ahead: the next node's T0^T k and T0^T q (tensor memory) and table values are
+            // in flight while the current node's ancestor sums run; only the stack reads wait on the previous
+            // node.  Tree mode walks the schedule's order; a chain segment its nodes in order.
+            float* sc_col = stk + c;
+            struct NodeVals {
+              int t, d, i0;
+              float k1, k2, q1, q2, vt, htt;
+              float4 sc;
+            };
+            auto fetch = [&](int w, NodeVals& x) {
+              if (CHAIN) {
+                x.t = s0 + w;
+                x.d = w;
+                x.i0 = coff[x.t];
+              } else {
+                const int pkw = __shfl_sync(FULL, wpack, w);
+                x.t = pkw & 0xFF;
+                x.d = (pkw >> 8) & 0xFF;
+                x.i0 = pkw >> 16;
+              }
+              const uint32_t tc = tD + static_cast<uint32_t>(x.t - s0);
+              x.k1 = tmem_ld1(tc);
+              x.k2 = tmem_ld1(tc + 2u * NBs);
+              x.q1 = tmem_ld1(tc + static_cast<uint32_t>(NBs));
+              x.q2 = tmem_ld1(tc + 3u * NBs);
+              x.sc = hsc[x.t];
+              x.vt = vcol[x.t * DV];
+              x.htt = hd[x.t];
+            };
+            NodeVals cv;
+            fetch(0, cv);
+            tmem_wait_ld();
+            for (int w = 0; w < ns; ++w) {
+              NodeVals nv;
+              if (w + 1 < ns) fetch(w + 1, nv);
+              float su = 0.f, so = 0.f;
+#pragma unroll 4
+              for (int m = 0; m < cv.d; ++m) {   // m-th ancestor (parent first) sits at depth d - 1 - m
+                const float4 e4 = ptab[cv.i0 + m];
+                const float us = sc_col[(cv.d - 1 - m) * DV];
+                su = fmaf(e4.x, us, su);
+                so = fmaf(e4.y, us, so);
+              }
+              const float u = fmaf(-cv.sc.z, cv.k1 + cv.k2, cv.sc.y * cv.vt) - su;
+              const float o = fmaf(cv.htt, u, fmaf(cv.sc.w, cv.q1 + cv.q2, so));
+              sc_col[cv.d * DV] = u;
+              vcol[cv.t * DV] = u;   // the u rows by node, for the boundary replay and the segment fold
+              u_col[cv.t * ostride] = u;
+              o_col[cv.t * ostride] = o;
+              tmem_wait_ld();
+              if (w + 1 < ns) cv = nv;
+            }
+            // a chain segment that is not the last: the running state absorbs it with the fold's operations
+            // (k rows from the staged rows, u rows just formed), T <- g T + k u^T node by node
+            if (CHAIN && !last) {
+              float gs = 1.f;
+              for (int w = 0; w < ns; ++w) {
+                const int t = s0 + w;
+                gs = fold_node(R, stg + t * DK, gs * hsc[t].x, vcol[t * DV]);
+              }
+              R.materialise(gs);
+            }
+          }
+          tmem_fence_before();
+          if (!CHAIN) break;
+        }
+        }
+        if (!ok) break;
 
         // ---- boundary states on request, replayed from T0 with the fold's operations and materialisation
         // points (k rows from the bank, u rows from shared memory), so a later fold reproduces them bit for bit
@@ -714,6 +926,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         group_sync(gid);
         if (has_nx) issue_rows(nxi, nxh);
       }
+      if (CHAIN && ok && nxt.it < n_items) issue_kq(nxt);   // (the last head ended on a group barrier)
       k += NG;
       cur = nxt;
     }
@@ -737,13 +950,13 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
   }
 }
 
-template <int DK, typename InT, int NG>
+template <int DK, typename InT, int NG, bool CHAIN>
 cudaError_t launch_tcp_t(const VerifyParams& p, cudaStream_t s) {
-  const PLayout L{p.n_max, DK};
+  const PLayout L{p.n_max, DK, CHAIN ? kPSeg : p.n_max};
   // at least half an SM's shared memory, so one CTA (and one tensor-memory allocation) per SM
   const size_t smem = L.bytes(NG) > 116 * 1024 ? static_cast<size_t>(L.bytes(NG)) : 116 * 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kern = ut_tcp_verify_kernel<DK, InT, NG>;
+  auto kern = ut_tcp_verify_kernel<DK, InT, NG, CHAIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -761,33 +974,35 @@ cudaError_t launch_tcp_t(const VerifyParams& p, cudaStream_t s) {
 }
 
 template <int DK, typename InT>
-cudaError_t launch_tcp_groups(const VerifyParams& p, cudaStream_t s) {
-  const PLayout L{p.n_max, DK};
-  if (L.bytes(2) <= 227 * 1024) return launch_tcp_t<DK, InT, 2>(p, s);
-  return launch_tcp_t<DK, InT, 1>(p, s);
+cudaError_t launch_tcp_groups(const VerifyParams& p, bool chain, cudaStream_t s) {
+  if (chain) return launch_tcp_t<DK, InT, 1, true>(p, s);   // one group: the staged rows serve every segment
+  const PLayout L{p.n_max, DK, p.n_max};
+  if (L.bytes(2) <= 227 * 1024) return launch_tcp_t<DK, InT, 2, false>(p, s);
+  return launch_tcp_t<DK, InT, 1, false>(p, s);
 }
 
 template <typename InT>
-cudaError_t launch_tcp_dtype(const VerifyParams& p, cudaStream_t s) {
+cudaError_t launch_tcp_dtype(const VerifyParams& p, bool chain, cudaStream_t s) {
   switch (p.dk) {
-    case 32: return launch_tcp_groups<32, InT>(p, s);
-    case 64: return launch_tcp_groups<64, InT>(p, s);
-    case 128: return launch_tcp_groups<128, InT>(p, s);
+    case 32: return launch_tcp_groups<32, InT>(p, chain, s);
+    case 64: return launch_tcp_groups<64, InT>(p, chain, s);
+    case 128: return launch_tcp_groups<128, InT>(p, chain, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-bool verify_tcp_supported(int dk, int dv, int n_max) {
-  if (dv != kPDv || !(dk == 32 || dk == 64 || dk == 128) || n_max < 1 || n_max > kPMaxNodes) return false;
-  return PLayout{n_max, dk}.bytes(1) <= 227 * 1024;
+bool verify_tcp_supported(int dk, int dv, int n_max, bool chain) {
+  if (dv != kPDv || !(dk == 32 || dk == 64 || dk == 128) || n_max < 1) return false;
+  if (n_max > (chain ? kPMaxChain : kPMaxNodes)) return false;
+  return PLayout{n_max, dk, chain ? kPSeg : n_max}.bytes(1) <= 227 * 1024;
 }
 
-cudaError_t launch_verify_tcp(const VerifyParams& p, cudaStream_t s) {
-  if (!verify_tcp_supported(p.dk, p.dv, p.n_max)) return cudaErrorInvalidValue;
-  if (p.in_dtype == GDN_DTYPE_BF16) return launch_tcp_dtype<__nv_bfloat16>(p, s);
-  return launch_tcp_dtype<float>(p, s);
+cudaError_t launch_verify_tcp(const VerifyParams& p, bool chain, cudaStream_t s) {
+  if (!verify_tcp_supported(p.dk, p.dv, p.n_max, chain)) return cudaErrorInvalidValue;
+  if (p.in_dtype == GDN_DTYPE_BF16) return launch_tcp_dtype<__nv_bfloat16>(p, chain, s);
+  return launch_tcp_dtype<float>(p, chain, s);
 }
 
 }  // namespace gdn

@@ -98,11 +98,12 @@ class TreeVerifier:
 
     def verify(self, sched: DeviceSchedule, x_raw, conv_w, beta, log_g, state, conv_state, out_o, boundary,
                stream=None, boundary_scratch: bool = False, chain_walk: bool = False, ut_simt: bool = False,
-               tc_per_head: bool = False):
+               tc_per_head: bool = False, chains: bool = False):
         flags = (N.GDN_VERIFY_BOUNDARY_SCRATCH if boundary_scratch else 0) | \
                 (N.GDN_VERIFY_CHAIN_WALK if chain_walk else 0) | \
                 (N.GDN_VERIFY_UT_SIMT if ut_simt else 0) | \
-                (N.GDN_VERIFY_TC_PER_HEAD if tc_per_head else 0)
+                (N.GDN_VERIFY_TC_PER_HEAD if tc_per_head else 0) | \
+                (N.GDN_VERIFY_CHAINS if chains else 0)
         N.gdn_tree_verify(self.dims, self.layers, sched.struct, x_raw, conv_w, beta, log_g, state, conv_state,
                           out_o, boundary, self.banks, self.workspace, self.ws_bytes, flags, stream)
 

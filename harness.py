@@ -38,6 +38,7 @@ class WorkloadPlan:
         self.chain_walk = chain_walk or per_node   # walk the schedule's chains (else the tree-masked UT form)
         self.ut_simt = ut_simt     # the UT form on the CUDA cores even where the tensor-core kernel applies
         self.tc_per_head = tc_per_head   # the tensor-core UT form with a CTA per v-head instead of the persistent one
+        self.chains = False        # every tree is a chain: long chains solved in segments on the tensor cores
         self.depth_hint = True   # pass the trees' depth, which sends trees deeper than GDN_UT_MAX_DEPTH to the walk
         self.trees = trees if trees is not None else [S.step_trees(w, s) for s in range(w.steps)]
         self.paths = paths if paths is not None else [S.step_paths(w, self.trees[s], s) for s in range(w.steps)]
@@ -119,7 +120,7 @@ class GpuSession:
         X, BE, AG = self.step_inputs(step)
         self.ver.verify(self.schedule(step), X, self.conv_w, BE, AG, self.state, self.conv_state, self.out_o,
                         self.boundary, stream, boundary_scratch, self.plan.chain_walk, self.plan.ut_simt,
-                        self.plan.tc_per_head)
+                        self.plan.tc_per_head, self.plan.chains)
 
     def local_layer(self, l: int) -> int:
         return self.layer_ids.index(l)

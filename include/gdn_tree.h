@@ -253,6 +253,9 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
 #define GDN_VERIFY_CHAIN_WALK 2         /* walk the heavy-light chains instead of the tree-masked UT form */
 #define GDN_VERIFY_UT_SIMT 4            /* UT form on the CUDA cores even where the tensor-core kernel applies */
 #define GDN_VERIFY_TC_PER_HEAD 8        /* tensor-core UT form with one CTA per v-head instead of the persistent kernel */
+#define GDN_VERIFY_CHAINS 16            /* every tree is a pure chain (parent[i] = i - 1): chains of up to 64 nodes are
+                                           solved on the tensor cores in 16-node segments (d_v = 128); a tree that is
+                                           not a chain sets GDN_DEVERR_SCHEDULE and is skipped */
 
 /* ---------------------------------------------------------------------------
  * gdn_tree_verify -- fold the pending path, then verify a batch of trees.
@@ -278,7 +281,8 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              With GDN_VERIFY_BOUNDARY_SCRATCH in flags it is scratch instead: only
  *              stashes that spill out of tensor memory are written there, and its
  *              contents are unspecified on return.
- *   flags      GDN_VERIFY_BOUNDARY_SCRATCH, GDN_VERIFY_CHAIN_WALK, GDN_VERIFY_UT_SIMT (other
+ *   flags      GDN_VERIFY_BOUNDARY_SCRATCH, GDN_VERIFY_CHAIN_WALK, GDN_VERIFY_UT_SIMT,
+ *              GDN_VERIFY_TC_PER_HEAD, GDN_VERIFY_CHAINS (other
  *              bits: GDN_ERR_INVALID_ARG).  By default the nodes are solved in the tree-masked
  *              UT form (article "状态驻留验证": the topology-masked UT decomposition): the
  *              committed state times every node's k and q, with no dependency between nodes,
@@ -289,7 +293,11 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              in registers, branch states stashed in tensor memory.  All give the same results
  *              up to rounding.  Batches whose sched->depth_max exceeds GDN_UT_MAX_DEPTH walk
  *              chains without the flag: the UT form's per-node work grows with the square of
- *              the depth.
+ *              the depth.  GDN_VERIFY_CHAINS (the caller guarantees that every tree is a chain)
+ *              solves chains of up to 64 nodes in the chunked UT form instead (SpecLA article,
+ *              "想深入源码": the chunked Gated DeltaNet form): each 16-node segment is solved
+ *              from the running state on the tensor cores, which then absorbs the segment with
+ *              the fold's operations.
  *   banks      factors of every node are written into bank write_bank
  *   workspace  >= gdn_workspace_bytes(d, B, layers, n_max) bytes of device memory
  * Rows of nodes >= n[b] are neither read nor written.

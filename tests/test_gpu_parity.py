@@ -225,15 +225,48 @@ def test_qwen_like_single_layer(kernel):
     run_parity(w, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", ["ut", "walk"])
+@pytest.mark.parametrize("kernel", ["chains_tc", "ut", "walk"])
 def test_chain64_single_layer(kernel):
-    # the pure-chain shape of the stress workload: 64-node chain, chain acceptance of the whole walk
-    # the UT form would hand a 63-deep chain to the walk; here it is made to solve it itself
+    # the pure-chain shape of the stress workload: 64-node chain, chain acceptance of the whole walk.
+    # "chains_tc": the caller declares every tree a chain, and the tensor cores solve it in 16-node segments;
+    # "ut": the UT form would hand a 63-deep chain to the walk; here it is made to solve it itself
     from harness import WorkloadPlan
     w = S.workload(6).replace(B=2, layers=1, steps=2)
     plan = WorkloadPlan(w)
     plan.depth_hint = kernel == "walk"
-    run_parity(w, plan=plan, kernel=kernel)
+    plan.chains = kernel == "chains_tc"
+    run_parity(w, plan=plan, kernel="ut" if kernel == "chains_tc" else kernel)
+
+
+@pytest.mark.parametrize("n_chain", [1, 5, 16, 17, 31, 33, 48, 64])
+def test_chain_segments_ragged(n_chain):
+    # chains of every segment shape (one partial segment, exact multiples of 16, a last segment of 1 node),
+    # several requests and layers, commits of the whole chain and of a prefix, 128-wide and 64-wide keys
+    from harness import WorkloadPlan
+    for dk in (128, 64):
+        w = S.workload(6).replace(B=3, layers=2, steps=3, Hk=2, Hv=6, dk=dk, budget=n_chain, n_max=64)
+        rng = np.random.default_rng(n_chain)
+        trees = [[S.chain_tree(n_chain) for _ in range(w.B)] for _ in range(w.steps)]
+        paths = [[np.arange(int(rng.integers(0, n_chain + 1)), dtype=np.int32) for _ in range(w.B)]
+                 for _ in range(w.steps)]
+        plan = WorkloadPlan(w, trees, paths)
+        plan.chains = True
+        run_parity(w, plan=plan)
+
+
+def test_chains_flag_refuses_a_tree():
+    # a tree that is not a chain under GDN_VERIFY_CHAINS is skipped with a schedule error, not solved wrongly
+    from harness import GpuSession, WorkloadPlan
+    import gated_deltanet_tree_gb300 as G
+    w = S.workload(6).replace(B=2, layers=1, steps=1, Hk=2, Hv=6, budget=40, n_max=40)
+    trees = [[S.chain_tree(40), np.array([-1] + [0] * 39, dtype=np.int32)]]
+    plan = WorkloadPlan(w, trees, [[np.arange(3, dtype=np.int32), np.zeros(0, dtype=np.int32)]])
+    plan.chains = True
+    gs = GpuSession(w, plan)
+    gs.verify(0)
+    with pytest.raises(G.GdnError) as e:
+        gs.ver.check_error()
+    assert e.value.status == G._native.GDN_ERR_SCHEDULE
 
 
 @pytest.mark.parametrize("kernel", ["ut", "walk"])
@@ -284,6 +317,7 @@ def test_stress_128_requests_layer_chunked(cfg):
     w = S.workload(cfg).replace(steps=3)
     from harness import WorkloadPlan
     plan = WorkloadPlan(w)
+    plan.chains = cfg == 6   # the pure chains in 16-node segments on the tensor cores
     for layers, units in ((range(0, 8), [(0, 0), (127, 5)]), (range(40, 48), [(77, 41), (3, 47)])):
         run_parity(w, units=units, plan=plan, layer_ids=layers)
 
