@@ -206,6 +206,19 @@ def tc_mma_shapes(w: S.Workload, n: int):
     return per_step * (w.dk // 8)
 
 
+CHAIN_SEG = 16   # GDN_VERIFY_CHAINS: nodes per segment
+
+
+def chain_tensor_flops(w: S.Workload, n_per_req):
+    """tf32 FLOPs of the chain-segment MMAs in one call: per segment of m nodes, the tree kernel's two
+    products for a tree of m nodes."""
+    per_head = 0
+    for n in n_per_req:
+        for s0 in range(0, n, CHAIN_SEG):
+            per_head += sum(2 * m * nn * k for m, nn, k in tc_mma_shapes(w, min(CHAIN_SEG, n - s0)))
+    return per_head * w.layers * w.Hv
+
+
 def tensor_flops(w: S.Workload, n_per_req):
     """tf32 FLOPs the tensor cores execute in one verify call (2 M N K per MMA)."""
     per_head = sum(sum(2 * m * nn * k for m, nn, k in tc_mma_shapes(w, n)) for n in n_per_req)
@@ -741,6 +754,8 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
     # the tree-masked UT kernels store no state but the committed one with boundary states as scratch, and a
     # pure chain stashes nothing, so no boundary buffer is needed (nb_max = 0)
     dummy = torch.empty(16, **f32)
+    chains = w.tree == "chain" and w.dv == 128   # every tree a chain: 16-node segments on the tensor cores
+    flags = N.GDN_VERIFY_BOUNDARY_SCRATCH | (N.GDN_VERIFY_CHAINS if chains else 0)
 
     def one(i, ev=None):
         s = i % w.steps
@@ -749,7 +764,7 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
         if ev is not None:
             ev[0].record()
         N.gdn_tree_verify(dims, w.layers, sc, X, conv_w, BE, AG, state, conv_state, out_o, dummy, ver.banks,
-                          ver.workspace, ver.ws_bytes, N.GDN_VERIFY_BOUNDARY_SCRATCH, None)
+                          ver.workspace, ver.ws_bytes, flags, None)
         if ev is not None:
             ev[1].record()
         N.gdn_commit_fold(dims, w.layers, sc, pt[s][0], pt[s][1], 0, ver.banks, None)
@@ -769,24 +784,30 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
     ms = t0.elapsed_time(t1)
     vms = [a.elapsed_time(b) for a, b in evs]
     units = sum(sum(nreq[(warmup + k) % w.steps]) for k in range(steps)) * w.layers * w.Hv
-    byts, fmas, walked = [], [], False
+    byts, fmas, tflops, walked = [], [], [], False
     for k in range(steps):
         i = warmup + k
         s = i % w.steps
         prev = paths[(i - 1) % w.steps]
         L = [len(p) for p in prev]
         byts.append(algorithmic_bytes(w, nreq[s], [0] * w.B, L))
+        if chains:   # the running state absorbs every segment but the last; the products run on the tensor cores
+            fmas.append(algorithmic_fma(w, [0] * w.B, [n - ((n - 1) % CHAIN_SEG + 1) for n in nreq[s]], L))
+            tflops.append(chain_tensor_flops(w, nreq[s]))
+            continue
         walk = depth[s] > UT_MAX_DEPTH
         walked = walked or walk
         ups = ([int((np.bincount(p[1:], minlength=len(p)) > 0).sum()) if len(p) > 1 else 0 for p in trees[s]]
                if walk else [0] * w.B)
         fmas.append(algorithmic_fma(w, nreq[s] if (walk or not tc_applies(w)) else [0] * w.B, ups, L))
+        tflops.append(tensor_flops(w, nreq[s]) if (tc_applies(w) and not walk) else 0)
     peak, peak_kind = peaks()
     avg_v = statistics.mean(vms) / 1e3
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count, 2070.0)
     gbs = statistics.mean(byts) / avg_v / 1e9
     tf = 2 * statistics.mean(fmas) / avg_v / 1e12
-    kernel = ("chain_verify_kernel (heavy-light chain walk: depth > %d)" % UT_MAX_DEPTH if walked else
+    kernel = ("ut_tcp_verify_kernel (chains in %d-node segments on the tensor cores)" % CHAIN_SEG if chains else
+              "chain_verify_kernel (heavy-light chain walk: depth > %d)" % UT_MAX_DEPTH if walked else
               "ut_tcp_verify_kernel (tensor cores, persistent)" if tc_applies(w) else
               "ut_verify_kernel (tree-masked UT form, CUDA cores)")
     line = {"workload": w.name, "requests": w.B, "gdn_layers": w.layers, "tree": f"{w.budget}-node {w.tree}",
@@ -798,6 +819,10 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
             "alu": {"achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
                     "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x 2070 MHz",
                     "algorithmic_flops_per_call": 2 * statistics.mean(fmas)},
+            "tensor": None if not any(tflops) else {
+                "achieved": statistics.mean(tflops) / avg_v / 1e12, "peak": tf32_peak(), "unit": "TFLOP/s",
+                "frac": statistics.mean(tflops) / avg_v / 1e12 / tf32_peak(),
+                "tf32_flops_per_call": statistics.mean(tflops)},
             "bound": "alu" if tf / alu_peak > gbs / peak else "hbm",
             "inputs": "trees and paths from the host generators; activations, states and conv weights seeded on "
                       "the device with the same distributions; two activation sets alternate"}

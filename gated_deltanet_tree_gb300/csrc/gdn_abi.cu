@@ -202,22 +202,30 @@ gdn_status gdn_tree_verify(const gdn_dims* d, int32_t layers, const gdn_batch_sc
   // the UT form costs depth^2 per node and depth per (node, column): deep trees walk their chains, unless
   // the caller says every tree is a chain, which the tensor cores then solve in 16-node segments
   const bool chains_tc = (flags & GDN_VERIFY_CHAINS) && !(flags & (GDN_VERIFY_CHAIN_WALK | GDN_VERIFY_UT_SIMT)) &&
-                         gdn::verify_tcp_supported(d->dk, d->dv, n_max, true);
+                         gdn::verify_tcp_supported(d->dk, d->dv, n_max, 1);
   vp.chain_walk = !chains_tc && ((flags & GDN_VERIFY_CHAIN_WALK) || sched->depth_max > GDN_UT_MAX_DEPTH) ? 1 : 0;
   vp.fold = pend >= 0;
   if (pend >= 0) {
     vp.pend_k = banks->k[pend]; vp.pend_u = banks->u[pend]; vp.pend_a = banks->a[pend];
   }
   vp.pend_path = banks->pend_path; vp.pend_len = banks->pend_len; vp.err = banks->err;
+  // trees of 33 to 64 nodes, none deeper than 16 (as the packers report it): one segment on the tensor cores
+  const bool wide_tc = !chains_tc && !vp.chain_walk && n_max > 32 && sched->depth_max >= 1 &&
+                       sched->depth_max <= gdn::kWideMaxDepth &&
+                       !(flags & (GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD)) &&
+                       gdn::verify_tcp_supported(d->dk, d->dv, n_max, 2);
   if (chains_tc) {
-    e = gdn::launch_verify_tcp(vp, true, stream);
+    e = gdn::launch_verify_tcp(vp, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, chain segments)");
+  } else if (wide_tc) {
+    e = gdn::launch_verify_tcp(vp, 2, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, up to 64 nodes)");
   } else if (vp.chain_walk) {
     e = gdn::launch_verify(vp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "chain-verify launch");
   } else if (!(flags & (GDN_VERIFY_UT_SIMT | GDN_VERIFY_TC_PER_HEAD)) &&
-             gdn::verify_tcp_supported(d->dk, d->dv, n_max, false)) {
-    e = gdn::launch_verify_tcp(vp, false, stream);
+             gdn::verify_tcp_supported(d->dk, d->dv, n_max, 0)) {
+    e = gdn::launch_verify_tcp(vp, 0, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tree-verify launch (tensor cores, persistent)");
   } else if (!(flags & GDN_VERIFY_UT_SIMT) && gdn::verify_tc_supported(d->dk, d->dv, n_max)) {
     e = gdn::launch_verify_tc(vp, stream);

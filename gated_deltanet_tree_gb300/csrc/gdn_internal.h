@@ -152,9 +152,11 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);      // chain 
 cudaError_t launch_verify_ut(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, CUDA cores
 cudaError_t launch_verify_tc(const VerifyParams& p, cudaStream_t s);   // tree-masked UT form, tensor cores, a CTA per head
 bool verify_tc_supported(int dk, int dv, int n_max);
-// the same, persistent and warp-specialised; chain: every tree is a pure chain, solved in 16-node segments
-cudaError_t launch_verify_tcp(const VerifyParams& p, bool chain, cudaStream_t s);
-bool verify_tcp_supported(int dk, int dv, int n_max, bool chain);
+// the same, persistent and warp-specialised.  mode 0: trees of up to 32 nodes; 1: every tree a pure chain of
+// up to 64 nodes, solved in 16-node segments; 2: trees of up to 64 nodes and depth at most 16
+cudaError_t launch_verify_tcp(const VerifyParams& p, int mode, cudaStream_t s);
+bool verify_tcp_supported(int dk, int dv, int n_max, int mode);
+constexpr int kWideMaxDepth = 16;   // deepest node mode 2 takes
 
 cudaError_t launch_commit(const CommitParams& p, int compact, cudaStream_t s);
 bool verify_supported(int dk, int dv);

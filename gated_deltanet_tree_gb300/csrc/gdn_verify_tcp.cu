@@ -61,6 +61,8 @@ constexpr int kPFold = 8;          // pending rows staged per fold chunk
 constexpr int kPMaxNodes = 32;     // 4 NB <= 128 D columns
 constexpr int kPSeg = 16;          // chain mode: nodes per segment
 constexpr int kPMaxChain = 64;     // chain mode: longest chain
+constexpr int kPMaxWide = 64;      // wide mode: largest tree
+constexpr int kPWideDepth = 16;    // wide mode: deepest node
 
 // ---- small PTX helpers
 // One non-blocking test of phase `parity` of `bar`.
@@ -138,21 +140,24 @@ __device__ __forceinline__ float tmem_ld1(uint32_t ta) {
 // nodes solved at once (the whole tree, or a chain segment): the operand, the depth stack and a segment's
 // pairs are sized by it; rows and per-node tables by n_max.
 struct PLayout {
-  int n_max, dk, seg;
+  int n_max, dk, seg, mode;
   __host__ __device__ static int a16(int x) { return (x + 15) & ~15; }
   __host__ __device__ int nbm() const { return (seg + 7) & ~7; }
-  // ancestor pairs inside segments, over all segments of an n_max-node tree or chain
+  // ancestor pairs inside segments, over all segments of an n_max-node tree or chain (wide mode: a node has
+  // at most kPWideDepth ancestors)
   __host__ __device__ int pairs() const {
+    if (mode == 2) return n_max * kPWideDepth;
     const int full = n_max / seg, r = n_max % seg;
     return full * (seg * (seg - 1) / 2) + r * (r - 1) / 2;
   }
+  __host__ __device__ int depths() const { return mode == 2 ? kPWideDepth + 1 : seg; }   // stack entries
   __host__ __device__ int words() const { return 5 + 4 * n_max; }
   // one group's region
   __host__ __device__ int opnd() const { return 0; }                                 // [dk/4][4 NB][16 B] operand
   __host__ __device__ int stg() const { return opnd() + 4 * nbm() * dk * 4; }         // [2][n_max][dk] k, q rows
-  __host__ __device__ int vbuf() const { return stg() + 2 * n_max * dk * 4; }         // [n_max][128] v, then u
-  __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [seg][128] u by depth
-  __host__ __device__ int pk() const { return stk() + seg * kPDv * 4; }               // [kPFold][dk] pending k
+  __host__ __device__ int vbuf() const { return stg() + (mode == 2 ? 0 : 2 * n_max * dk * 4); }   // [n_max][128] v, u
+  __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [depths][128] u by depth
+  __host__ __device__ int pk() const { return stk() + depths() * kPDv * 4; }          // [kPFold][dk] pending k
   __host__ __device__ int pu() const { return pk() + kPFold * dk * 4; }               // [kPFold][128] pending u
   __host__ __device__ int ptab() const { return pu() + kPFold * kPDv * 4; }           // [pairs] (A, C, s dv, -)
   __host__ __device__ int hsc() const { return ptab() + a16(pairs() * 16); }          // [n_max] (g, beta, bG, G)
@@ -172,16 +177,19 @@ struct PLayout {
   __host__ __device__ int bytes(int ng) const { return shared(ng) + ng * 4 * 8 + 16; }
 };
 
-// CHAIN: every tree is a pure chain (parent[i] = i - 1), solved in segments of kPSeg nodes: each segment is
-// a chain in the UT form from the running state, which then absorbs the segment by the fold's operations
-// (the chunked UT form of a long chain); otherwise the whole tree is one segment (n_max <= 32).
-template <int DK, typename InT, int NG, bool CHAIN>
+// Modes.  0: trees of up to 32 nodes, the whole tree one segment, k and q rows staged by TMA.  1 (chain):
+// every tree is a pure chain (parent[i] = i - 1), solved in segments of kPSeg nodes: each segment is a chain
+// in the UT form from the running state, which then absorbs the segment by the fold's operations (the
+// chunked UT form of a long chain).  2 (wide): trees of up to 64 nodes and depth at most kPWideDepth, one
+// segment, the operand built straight from global memory (no staging copy), one group per SM.
+template <int DK, typename InT, int NG, int MODE>
 __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyParams p, int n_items, int hpi) {
+  constexpr bool CHAIN = MODE == 1, WIDE = MODE == 2;
   constexpr int DV = kPDv;
   constexpr int KC = DK / 4;                    // 16-byte chunks of a k or q row
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char smem[];
-  const PLayout L{p.n_max, DK, CHAIN ? kPSeg : p.n_max};
+  const PLayout L{p.n_max, DK, CHAIN ? kPSeg : p.n_max, MODE};
   const int SEG = CHAIN ? kPSeg : p.n_max;      // nodes per segment
   const int n_max = p.n_max;
   const int tid = threadIdx.x;
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
 
   if (warp == 0) {
     __syncwarp();
-    tmem_alloc(tslot, NG * 256);
+    tmem_alloc(tslot, WIDE ? 512 : NG * 256);   // (wide mode: A 128 columns + D up to 256)
     tmem_relinquish();
   }
   if (tid == 32) {
@@ -262,6 +270,15 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
     };
     // ---- TMA issue, warp 0 of the group (all lanes call; lane 0 arms the barrier)
     auto issue_kq = [&](const Item& x) {   // k and q rows of all n_max node slots of the item's k-head
+      if (WIDE) {   // (wide mode reads them from global memory when it builds the operand: into L2 now)
+        if (wq == 0)
+          for (int node = lane; node < n_max; node += 32) {
+            const size_t row = static_cast<size_t>(x.bl) * n_max + node;
+            prefetch_l2(p.k_in + (row * p.Hk + x.kh) * DK, DK * 4);
+            prefetch_l2(p.q_in + (row * p.Hk + x.kh) * DK, DK * 4);
+          }
+        return;
+      }
       if (wq == 0) {
         if (lane == 0) mbar_expect(b_kq, static_cast<uint32_t>(2 * n_max * DK * 4));
         __syncwarp();
@@ -308,11 +325,12 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
     };
     // ---- per-item words held in registers until the item starts: schedule record, pending path entry c,
     // pending length (-1: out of range)
-    int rw0 = 0, rw1 = 0, pth_nx = 0, lp_nx = 0;
+    int rw0 = 0, rw1 = 0, rw2 = 0, pth_nx = 0, lp_nx = 0;   // (rw2: records of more than 256 words, n_max > 62)
     auto load_item_regs = [&](const Item& x) {
       const int32_t* r = p.words + static_cast<size_t>(x.b) * lay.words();
       rw0 = c < lay.words() ? r[c] : 0;
       rw1 = c + kPGroup < lay.words() ? r[c + kPGroup] : 0;
+      if (MODE != 0) rw2 = c + 2 * kPGroup < lay.words() ? r[c + 2 * kPGroup] : 0;
       int lp = p.fold ? p.pend_len[x.b] : 0;
       pth_nx = (p.fold && c < n_max) ? p.pend_path[static_cast<size_t>(x.b) * n_max + c] : 0;
       // an entry past n_max would address outside the banks: the whole path is refused
@@ -374,6 +392,26 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       }
       fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
     };
+    // wide mode: the same operand from the k rows (factor bank) and q rows (workspace) in global memory
+    auto build_operand_g = [&](const Item& x, int ns, int NB) {
+      const size_t row0 = static_cast<size_t>(x.bl) * n_max;
+      for (int job = c; job < 2 * NB * KC; job += kPGroup) {
+        const int r = job / KC, kc = job % KC;
+        const bool isq = r >= NB;
+        const int node = isq ? r - NB : r;
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (node < ns)
+          x4 = __ldg(reinterpret_cast<const float4*>((isq ? p.q_in : p.k_in) + ((row0 + node) * p.Hk + x.kh) * DK) + kc);
+        float4 hi, lo;
+        hi.x = tf32_hi(x4.x); lo.x = tf32_lo(x4.x);
+        hi.y = tf32_hi(x4.y); lo.y = tf32_lo(x4.y);
+        hi.z = tf32_hi(x4.z); lo.z = tf32_lo(x4.z);
+        hi.w = tf32_hi(x4.w); lo.w = tf32_lo(x4.w);
+        *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
+        *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+      }
+      fence_proxy_async();
+    };
     // parent inside the node's segment (-1 at a segment's first node)
     auto spar = [&](int v) { return CHAIN ? (v % kPSeg ? v - 1 : -1) : rec[lay.parent() + v]; };
 
@@ -397,6 +435,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       if (!ok) break;
       if (c < lay.words()) rec[c] = rw0;   // (the record is shorter than the group: the path follows it)
       if (c + kPGroup < lay.words()) rec[c + kPGroup] = rw1;
+      if (MODE != 0 && c + 2 * kPGroup < lay.words()) rec[c + 2 * kPGroup] = rw2;
       if (c < n_max) spath[c] = pth_nx;
       const int pth_cur = pth_nx;
       const int Lraw = lp_nx;
@@ -408,13 +447,16 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         item_ok = c == 0 ? parent[0] == -1 : (CHAIN ? parent[c] == c - 1 : (parent[c] >= 0 && parent[c] < c));
       item_ok = group_and(gid, item_ok);
       if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
-      ok = group_and(gid, mbar_wait_ab(b_kq, ph_kq, abortw));
-      if (!ok) break;   // (still armed: the drain below waits for the copy)
-      ph_kq ^= 1;
-      armed_kq = false;
+      if (!WIDE) {
+        ok = group_and(gid, mbar_wait_ab(b_kq, ph_kq, abortw));
+        if (!ok) break;   // (still armed: the drain below waits for the copy)
+        ph_kq ^= 1;
+        armed_kq = false;
+      }
       const int NB = (n + 7) & ~7;   // (tree mode: the whole tree is one segment)
       if (item_ok) {
-        if (!CHAIN) build_operand(0, n, NB);
+        if (MODE == 0) build_operand(0, n, NB);
+        if (WIDE) build_operand_g(cur, n, NB);
         // depths and pair offsets (warp 0, a lane per node), then every node's ancestors; in chain mode the
         // depth inside a segment and the offsets have closed forms
         if (CHAIN) {
@@ -430,6 +472,31 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
             }
           }
           if (c == 0) coff[n] = (n / kPSeg) * sp + (n % kPSeg) * (n % kPSeg - 1) / 2;
+        } else if (WIDE) {
+          // up to 64 nodes: a thread per node for the depths, then each node's pair offset (the depths before
+          // it) and its ancestors; a node deeper than kPWideDepth refuses the item
+          bool shallow = true;
+          for (int t = c; t < n; t += kPGroup) {
+            int d = 0;
+            for (int v = t; v > 0; v = parent[v]) ++d;
+            dep[t] = d;
+            shallow = shallow && d <= kPWideDepth;
+          }
+          item_ok = group_and(gid, shallow);
+          if (item_ok) {
+            for (int t = c; t < n; t += kPGroup) {
+              int o = 0;
+              for (int v = 0; v < t; ++v) o += dep[v];
+              coff[t] = o;
+              for (int v = parent[t]; v >= 0; v = parent[v], ++o) {
+                ranc[o] = v;
+                ptn[o] = t;
+              }
+              if (t == n - 1) coff[n] = o;
+            }
+          } else if (c == 0) {
+            device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
+          }
         } else if (wq == 0) {
           int d = 0;
           if (lane < n)
@@ -458,8 +525,54 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       // every warp holds walk position w: node | depth << 8 | pair offset << 16.  The order is checked: every
       // node once, the root first, the depth rising by at most one per step, and each node's parent the last
       // node visited one level up (so the stack always holds the current node's root path).
-      int wpack = 0;
-      if (!CHAIN && item_ok) {
+      int wpack = 0, wpack1 = 0;   // (wide mode: lane w holds walk positions w and w + 32)
+      if (WIDE && item_ok) {
+        int tt[2], dd[2], pt[2];
+        bool in[2], good = true;
+        unsigned lo = 0u, hi = 0u;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int w = lane + 32 * h2;
+          tt[h2] = w < n ? (rec[lay.ops() + w] & kOpNode) : 0;
+          in[h2] = w < n && tt[h2] < n;
+          dd[h2] = in[h2] ? dep[tt[h2]] : 0;
+          good = good && (w >= n || in[h2]);
+          if (in[h2]) {
+            if (tt[h2] < 32) lo |= 1u << tt[h2];
+            else hi |= 1u << (tt[h2] - 32);
+          }
+          pt[h2] = in[h2] && w > 0 ? parent[tt[h2]] : -2;
+        }
+        lo = __reduce_or_sync(FULL, lo);
+        hi = __reduce_or_sync(FULL, hi);
+        good = good && __popc(lo) + __popc(hi) == n && (lane != 0 || tt[0] == 0);
+        // as in tree mode: the parent comes earlier and no position in between is shallower than the node
+        bool found[2] = {false, false};
+        int mind[2] = {1 << 20, 1 << 20};
+        for (int q = 0; q < 64; ++q) {
+          const int tq = __shfl_sync(FULL, q < 32 ? tt[0] : tt[1], q & 31);
+          const int dq = __shfl_sync(FULL, q < 32 ? dd[0] : dd[1], q & 31);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            if (q < lane + 32 * h2) {
+              if (tq == pt[h2]) {
+                found[h2] = true;
+                mind[h2] = 1 << 20;
+              } else {
+                mind[h2] = min(mind[h2], dq);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          if (in[h2] && lane + 32 * h2 > 0) good = good && found[h2] && mind[h2] >= dd[h2];
+        wpack = tt[0] | (dd[0] << 8) | ((in[0] ? coff[tt[0]] : 0) << 16);
+        wpack1 = tt[1] | (dd[1] << 8) | ((in[1] ? coff[tt[1]] : 0) << 16);
+        item_ok = group_and(gid, good);
+        if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
+      }
+      if (MODE == 0 && item_ok) {
         const int w = lane;
         const int t = w < n ? (rec[lay.ops() + w] & kOpNode) : 0;
         const bool in = w < n && t < n;
@@ -499,11 +612,18 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           const float4* kt = reinterpret_cast<const float4*>(stg + t * DK);
           const float4* qt = reinterpret_cast<const float4*>(stg + (n_max + t) * DK);
           const float4* ks = reinterpret_cast<const float4*>(stg + s * DK);
+          // (wide mode: the rows are the operand's high + low parts, which add up to the fp32 values exactly)
+          const float4* op4 = reinterpret_cast<const float4*>(opnd);
+          auto wrow = [&](int r, int kc) {
+            const float4 h4 = op4[kc * 4 * NB + r], l4 = op4[kc * 4 * NB + 2 * NB + r];
+            return make_float4(h4.x + l4.x, h4.y + l4.y, h4.z + l4.z, h4.w + l4.w);
+          };
           float sg[2] = {0.f, 0.f}, sh[2] = {0.f, 0.f};   // two partial sums each: shorter dependency chains
 #pragma unroll 8
           for (int q = 0; q < KC; ++q) {
             const int kc = (q + job) & (KC - 1);
-            const float4 a = kt[kc], b = qt[kc], e = ks[kc];
+            const float4 a = WIDE ? wrow(t, kc) : kt[kc], b = WIDE ? wrow(NB + t, kc) : qt[kc];
+            const float4 e = WIDE ? wrow(s, kc) : ks[kc];
             sg[q & 1] += fmaf(a.x, e.x, a.y * e.y) + fmaf(a.z, e.z, a.w * e.w);
             sh[q & 1] += fmaf(b.x, e.x, b.y * e.y) + fmaf(b.z, e.z, b.w * e.w);
           }
@@ -573,7 +693,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           issue_pend(nxi, nxh, min(kPFold, nx_lp), pe);
         }
 
-        if constexpr (!CHAIN) {
+        if constexpr (MODE == 0) {
         // ---- 2. A = T0^T, high part, and its product with all 4 NB operand rows
         if (item_ok) {
 #pragma unroll
@@ -839,7 +959,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
                 x.d = w;
                 x.i0 = coff[x.t];
               } else {
-                const int pkw = __shfl_sync(FULL, wpack, w);
+                const int pkw = __shfl_sync(FULL, w < 32 ? wpack : wpack1, w & 31);
                 x.t = pkw & 0xFF;
                 x.d = (pkw >> 8) & 0xFF;
                 x.i0 = pkw >> 16;
@@ -946,17 +1066,17 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
   __syncthreads();
   if (warp == 0) {
     tmem_fence_after();
-    tmem_dealloc(tbase, NG * 256);
+    tmem_dealloc(tbase, WIDE ? 512 : NG * 256);
   }
 }
 
-template <int DK, typename InT, int NG, bool CHAIN>
+template <int DK, typename InT, int NG, int MODE>
 cudaError_t launch_tcp_t(const VerifyParams& p, cudaStream_t s) {
-  const PLayout L{p.n_max, DK, CHAIN ? kPSeg : p.n_max};
+  const PLayout L{p.n_max, DK, MODE == 1 ? kPSeg : p.n_max, MODE};
   // at least half an SM's shared memory, so one CTA (and one tensor-memory allocation) per SM
   const size_t smem = L.bytes(NG) > 116 * 1024 ? static_cast<size_t>(L.bytes(NG)) : 116 * 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kern = ut_tcp_verify_kernel<DK, InT, NG, CHAIN>;
+  auto kern = ut_tcp_verify_kernel<DK, InT, NG, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -974,35 +1094,36 @@ cudaError_t launch_tcp_t(const VerifyParams& p, cudaStream_t s) {
 }
 
 template <int DK, typename InT>
-cudaError_t launch_tcp_groups(const VerifyParams& p, bool chain, cudaStream_t s) {
-  if (chain) return launch_tcp_t<DK, InT, 1, true>(p, s);   // one group: the staged rows serve every segment
-  const PLayout L{p.n_max, DK, p.n_max};
-  if (L.bytes(2) <= 227 * 1024) return launch_tcp_t<DK, InT, 2, false>(p, s);
-  return launch_tcp_t<DK, InT, 1, false>(p, s);
+cudaError_t launch_tcp_groups(const VerifyParams& p, int mode, cudaStream_t s) {
+  if (mode == 1) return launch_tcp_t<DK, InT, 1, 1>(p, s);   // one group: the staged rows serve every segment
+  if (mode == 2) return launch_tcp_t<DK, InT, 1, 2>(p, s);   // one group: its D columns take half of the SM's
+  const PLayout L{p.n_max, DK, p.n_max, 0};
+  if (L.bytes(2) <= 227 * 1024) return launch_tcp_t<DK, InT, 2, 0>(p, s);
+  return launch_tcp_t<DK, InT, 1, 0>(p, s);
 }
 
 template <typename InT>
-cudaError_t launch_tcp_dtype(const VerifyParams& p, bool chain, cudaStream_t s) {
+cudaError_t launch_tcp_dtype(const VerifyParams& p, int mode, cudaStream_t s) {
   switch (p.dk) {
-    case 32: return launch_tcp_groups<32, InT>(p, chain, s);
-    case 64: return launch_tcp_groups<64, InT>(p, chain, s);
-    case 128: return launch_tcp_groups<128, InT>(p, chain, s);
+    case 32: return launch_tcp_groups<32, InT>(p, mode, s);
+    case 64: return launch_tcp_groups<64, InT>(p, mode, s);
+    case 128: return launch_tcp_groups<128, InT>(p, mode, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-bool verify_tcp_supported(int dk, int dv, int n_max, bool chain) {
-  if (dv != kPDv || !(dk == 32 || dk == 64 || dk == 128) || n_max < 1) return false;
-  if (n_max > (chain ? kPMaxChain : kPMaxNodes)) return false;
-  return PLayout{n_max, dk, chain ? kPSeg : n_max}.bytes(1) <= 227 * 1024;
+bool verify_tcp_supported(int dk, int dv, int n_max, int mode) {
+  if (dv != kPDv || !(dk == 32 || dk == 64 || dk == 128) || n_max < 1 || mode < 0 || mode > 2) return false;
+  if (n_max > (mode == 1 ? kPMaxChain : mode == 2 ? kPMaxWide : kPMaxNodes)) return false;
+  return PLayout{n_max, dk, mode == 1 ? kPSeg : n_max, mode}.bytes(1) <= 227 * 1024;
 }
 
-cudaError_t launch_verify_tcp(const VerifyParams& p, bool chain, cudaStream_t s) {
-  if (!verify_tcp_supported(p.dk, p.dv, p.n_max, chain)) return cudaErrorInvalidValue;
-  if (p.in_dtype == GDN_DTYPE_BF16) return launch_tcp_dtype<__nv_bfloat16>(p, chain, s);
-  return launch_tcp_dtype<float>(p, chain, s);
+cudaError_t launch_verify_tcp(const VerifyParams& p, int mode, cudaStream_t s) {
+  if (!verify_tcp_supported(p.dk, p.dv, p.n_max, mode)) return cudaErrorInvalidValue;
+  if (p.in_dtype == GDN_DTYPE_BF16) return launch_tcp_dtype<__nv_bfloat16>(p, mode, s);
+  return launch_tcp_dtype<float>(p, mode, s);
 }
 
 }  // namespace gdn

@@ -269,10 +269,37 @@ def test_chains_flag_refuses_a_tree():
     assert e.value.status == G._native.GDN_ERR_SCHEDULE
 
 
-@pytest.mark.parametrize("kernel", ["ut", "walk"])
+@pytest.mark.parametrize("kernel", ["ut", "simt", "walk"])
 def test_ddtree64_top8_single_layer(kernel):
+    # the default dispatch ("ut") solves these 64-node, depth <= 16 trees on the tensor cores in one segment
     w = S.workload(5).replace(B=2, layers=1, steps=2)
     run_parity(w, kernel=kernel)
+
+
+def shallow_random_tree(n, rng, max_depth=16):
+    while True:
+        t = S.random_tree(n, rng)
+        d = np.zeros(n, dtype=np.int64)
+        for i in range(1, n):
+            d[i] = d[t[i]] + 1
+        if d.max() <= max_depth:
+            return t
+
+
+@pytest.mark.parametrize("dk", [128, 64])
+def test_wide_trees_ragged(dk):
+    # trees of 33 to 64 nodes (and smaller ones in the same batch) on the tensor cores: DDTrees, random trees,
+    # a star, a node at depth 16, boundary states stored and replayed, commits of every length
+    from harness import WorkloadPlan
+    n_max = 64
+    w = S.workload(5).replace(B=4, layers=2, steps=3, Hk=2, Hv=6, dk=dk, n_max=n_max, budget=n_max, path_max=n_max,
+                              tree="random")
+    rng = np.random.default_rng(41 + dk)
+    deep = np.array([-1] + list(range(16)) + [0] * 20, dtype=np.int32)   # a 16-deep chain plus a star
+    trees = [[S.ddtree(64, 8, 16, rng), shallow_random_tree(int(rng.integers(33, 65)), rng), deep,
+              shallow_random_tree(int(rng.integers(1, 33)), rng)] for _ in range(w.steps)]
+    paths = [[S.random_walk_path(t, rng, max_len=n_max) for t in ts] for ts in trees]
+    run_parity(w, plan=WorkloadPlan(w, trees, paths))
 
 
 # the method's degenerate cases, driven through every verify kernel: each variant below changes the Qwen-like
@@ -312,14 +339,15 @@ def test_batched_32x48_eight_steps(kernel):
 
 @pytest.mark.parametrize("cfg", [5, 6], ids=["ddtree64_top8", "chain64"])
 def test_stress_128_requests_layer_chunked(cfg):
-    # 128 requests x 48 layers of 64-node trees: the boundary states alone would take ~360 GB,
-    # so calls cover 8 layers at a time; the chunks holding the sampled units run all steps
-    w = S.workload(cfg).replace(steps=3)
+    # 128 requests x 48 layers of 64-node trees, all 8 verify -> commit steps: the boundary states alone would
+    # take ~360 GB, so a call covers 8 layers; the chunk holding the sampled units runs every step.  The
+    # top-8 trees run on the tensor cores in one segment, the pure chains in 16-node segments.
+    w = S.workload(cfg)
+    assert w.steps == 8
     from harness import WorkloadPlan
     plan = WorkloadPlan(w)
-    plan.chains = cfg == 6   # the pure chains in 16-node segments on the tensor cores
-    for layers, units in ((range(0, 8), [(0, 0), (127, 5)]), (range(40, 48), [(77, 41), (3, 47)])):
-        run_parity(w, units=units, plan=plan, layer_ids=layers)
+    plan.chains = cfg == 6
+    run_parity(w, units=[(0, 0), (127, 5)], plan=plan, layer_ids=range(0, 8))
 
 
 def test_checkpoint_resume_is_bitwise():
