@@ -190,10 +190,15 @@ def algorithmic_fma(w: S.Workload, n_per_req, updates_per_req, pend_len_per_req)
 
 
 TC_MAX_NODES = 32   # the tensor-core UT kernels take d_v = 128 and n_max <= 32 (gdn_tree_verify's dispatch)
+TC_WIDE_NODES, TC_WIDE_DEPTH = 64, 16   # ... and n_max <= 64 when no tree is deeper than 16
 
 
-def tc_applies(w: S.Workload) -> bool:
-    return w.dv == 128 and w.dk in (32, 64, 128) and w.n_max <= TC_MAX_NODES
+def tc_applies(w: S.Workload, depth_max: int = 0) -> bool:
+    """Whether gdn_tree_verify's default dispatch solves the batch on the tensor cores (depth_max: the packers'
+    deepest node of the batch, 0 when unknown)."""
+    if not (w.dv == 128 and w.dk in (32, 64, 128)):
+        return False
+    return w.n_max <= TC_MAX_NODES or (w.n_max <= TC_WIDE_NODES and 1 <= depth_max <= TC_WIDE_DEPTH)
 
 
 def tc_mma_shapes(w: S.Workload, n: int):
@@ -795,12 +800,13 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
             fmas.append(algorithmic_fma(w, [0] * w.B, [n - ((n - 1) % CHAIN_SEG + 1) for n in nreq[s]], L))
             tflops.append(chain_tensor_flops(w, nreq[s]))
             continue
-        walk = depth[s] > UT_MAX_DEPTH
+        tc = tc_applies(w, depth[s])
+        walk = depth[s] > UT_MAX_DEPTH and not tc
         walked = walked or walk
         ups = ([int((np.bincount(p[1:], minlength=len(p)) > 0).sum()) if len(p) > 1 else 0 for p in trees[s]]
                if walk else [0] * w.B)
-        fmas.append(algorithmic_fma(w, nreq[s] if (walk or not tc_applies(w)) else [0] * w.B, ups, L))
-        tflops.append(tensor_flops(w, nreq[s]) if (tc_applies(w) and not walk) else 0)
+        fmas.append(algorithmic_fma(w, nreq[s] if (walk or not tc) else [0] * w.B, ups, L))
+        tflops.append(tensor_flops(w, nreq[s]) if tc else 0)
     peak, peak_kind = peaks()
     avg_v = statistics.mean(vms) / 1e3
     alu_peak = fp32_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count, 2070.0)
@@ -808,7 +814,7 @@ def run_config(cfg: int, dev, steps: int = 6, warmup: int = 3):
     tf = 2 * statistics.mean(fmas) / avg_v / 1e12
     kernel = ("ut_tcp_verify_kernel (chains in %d-node segments on the tensor cores)" % CHAIN_SEG if chains else
               "chain_verify_kernel (heavy-light chain walk: depth > %d)" % UT_MAX_DEPTH if walked else
-              "ut_tcp_verify_kernel (tensor cores, persistent)" if tc_applies(w) else
+              "ut_tcp_verify_kernel (tensor cores, persistent)" if tc_applies(w, max(depth)) else
               "ut_verify_kernel (tree-masked UT form, CUDA cores)")
     line = {"workload": w.name, "requests": w.B, "gdn_layers": w.layers, "tree": f"{w.budget}-node {w.tree}",
             "value": units / (ms / 1e3), "unit": UNIT, "steps": steps, "warmup": warmup,

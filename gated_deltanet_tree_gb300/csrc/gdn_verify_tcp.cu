@@ -718,7 +718,15 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           }
           armed_mma = true;
         }
-        if (item_ok && Lp > 0) R.store(st, DV);   // the committed state, written once, while the product runs
+        if (item_ok && Lp > 0) {   // the committed state, written once while the product runs (evict-first: read
+                                   // again only by the next call)
+#pragma unroll
+          for (int j2 = 0; j2 < DK / 2; ++j2) {
+            const float2 a2 = unpack2(R.T[j2]);
+            __stcs(st + static_cast<size_t>(2 * j2) * DV, a2.x);
+            __stcs(st + static_cast<size_t>(2 * j2 + 1) * DV, a2.y);
+          }
+        }
 
         // ---- 3. this head's coefficients: a thread of warp 1 per node walks its ancestors (rho by products,
         // no division), A_ts = beta_t rho_ts G_ts and C_ts = rho_ts H_ts into the pair table
@@ -829,8 +837,8 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
             const float o = fmaf(cv.htt, u, fmaf(cv.sc.w, cv.q1 + cv.q2, so));
             sc_col[cv.d * DV] = u;
             vcol[cv.t * DV] = u;   // the u rows by node, for the boundary replay
-            u_col[cv.t * ostride] = u;
-            o_col[cv.t * ostride] = o;
+            __stcs(u_col + cv.t * ostride, u);   // (streaming stores: nothing in this call reads them again)
+            __stcs(o_col + cv.t * ostride, o);
             tmem_wait_ld();
             if (w + 1 < n) cv = nv;
           }
