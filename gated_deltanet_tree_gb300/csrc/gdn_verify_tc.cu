@@ -664,7 +664,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) ut_tc_verify_kernel(VerifyParam
 template <int DK, typename InT>
 cudaError_t launch_tc_t(const VerifyParams& p, cudaStream_t s) {
   const TcSmem<DK> L{p.n_max};
-  const size_t smem = L.bytes();
+  // Each CTA holds kTcCols of the SM's 512 tensor-memory columns, so at most two may be resident: a third
+  // would wait inside tcgen05.alloc until one of them exits.  Asking for more than a third of the SM's
+  // 228 KB of shared memory keeps a third CTA off the SM (small d_k and n_max would otherwise fit three).
+  constexpr size_t kTwoPerSm = 80 * 1024;
+  const size_t smem = L.bytes() > kTwoPerSm ? L.bytes() : kTwoPerSm;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kern = ut_tc_verify_kernel<DK, InT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
