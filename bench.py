@@ -663,7 +663,7 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
 
     def run(nsteps):
         h2d_done = [ev() for _ in range(nsteps)]
-        cmp_done = [ev() for _ in range(nsteps)]
+        cmp_done = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]   # (also the step clock)
         d2h_done = [ev() for _ in range(nsteps)]
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -701,11 +701,16 @@ def run_e2e(args, w, gs, dev, stream, paths, parents_host, words_host, words_dev
         s_d2h.wait_event(d2h_done[nsteps - 1])
         e1.record(s_d2h)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1), units
+        # the interval between consecutive steps' compute ends: the pipeline's period, step by step
+        per = [cmp_done[k - 1].elapsed_time(cmp_done[k]) for k in range(1, nsteps)]
+        return e0.elapsed_time(e1), units, per
 
     run(warm)
-    ms, units = run(steps)
-    return dict(ms=ms, units=units, steps=steps, h2d=h2d, d2h=d2h)
+    ms, units, per = run(steps)
+    med = statistics.median(per) if per else float("nan")
+    return dict(ms=ms, units=units, steps=steps, h2d=h2d, d2h=d2h, step_ms_median=med,
+                step_ms_max=max(per) if per else float("nan"),
+                stalled_steps=sum(1 for x in per if x > 2.0 * med))
 
 
 def device_inputs(w: S.Workload, dev, seed: int):
@@ -954,7 +959,12 @@ def main():
             "value": r["e2e_units"] / (r["e2e_ms"] / 1e3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
             "host_per_step": ("DDTree construction from the draft tables, " if w.tree == "ddtree" else "")
-                             + "heavy-light schedules, packing"},
+                             + "heavy-light schedules, packing",
+            # rank 0's pipeline period step by step (uploads, compute and downloads overlap across steps):
+            # the median is the steady state; a stalled step took over twice the median (host-link stalls of
+            # tens of ms also hit plain pinned copies with no kernel running)
+            "step_ms_median": e2e.get("step_ms_median"), "step_ms_max": e2e.get("step_ms_max"),
+            "stalled_steps": e2e.get("stalled_steps")},
         "gpu_launches": r["gpu_launches"],
         "ab_boundary_output": None if r["bout"] is None else dict(
             r["bout"], cost_vs_scratch=r["bout"]["ms_per_step"] / (r["ms"] / args.steps)),
