@@ -981,6 +981,56 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
               x.vt = vcol[x.t * DV];
               x.htt = hd[x.t];
             };
+            if (CHAIN && ns == kPSeg) {
+              // a whole chain segment: every earlier node of the segment is an ancestor and the pair offsets are
+              // closed forms, so the substitution runs unrolled with u in registers.  Each sum takes the oldest
+              // ancestor first, so only its last term waits on the node just solved; the o sums, independent of
+              // each other, follow, and the stores come last.
+              float uu[kPSeg];
+              const int pb = coff[s0];   // the segment's pairs: node s0 + tl has them at pb + tl (tl - 1) / 2
+              const float* pa = reinterpret_cast<const float*>(ptab + pb);   // (A, C, -, -) per pair
+#pragma unroll
+              for (int t0 = 0; t0 < kPSeg; t0 += 8) {
+                float k1[8], k2[8];
+                tmem_ld8(tD + static_cast<uint32_t>(t0), k1);
+                tmem_ld8(tD + static_cast<uint32_t>(2 * NBs + t0), k2);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const float4 sc = hsc[s0 + t0 + jj];
+                  uu[t0 + jj] = fmaf(-sc.z, k1[jj] + k2[jj], sc.y * vcol[(s0 + t0 + jj) * DV]);
+                }
+              }
+#pragma unroll
+              for (int tl = 1; tl < kPSeg; ++tl) {
+                float su = 0.f;
+#pragma unroll
+                for (int sl = 0; sl < tl; ++sl) su = fmaf(pa[4 * (tl * (tl - 1) / 2 + (tl - 1 - sl))], uu[sl], su);
+                uu[tl] -= su;
+              }
+#pragma unroll
+              for (int t0 = 0; t0 < kPSeg; t0 += 8) {
+                float q1[8], q2[8], oo[8];
+                tmem_ld8(tD + static_cast<uint32_t>(NBs + t0), q1);
+                tmem_ld8(tD + static_cast<uint32_t>(3 * NBs + t0), q2);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const int tl = t0 + jj, t = s0 + tl;
+                  float so = 0.f;
+#pragma unroll
+                  for (int sl = 0; sl < tl; ++sl) so = fmaf(pa[4 * (tl * (tl - 1) / 2 + (tl - 1 - sl)) + 1], uu[sl], so);
+                  oo[jj] = fmaf(hd[t], uu[tl], fmaf(hsc[t].w, q1[jj] + q2[jj], so));
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const int t = s0 + t0 + jj;
+                  vcol[t * DV] = uu[t0 + jj];   // the u rows by node, for the segment fold
+                  u_col[t * ostride] = uu[t0 + jj];
+                  o_col[t * ostride] = oo[jj];
+                }
+              }
+            } else {
             NodeVals cv;
             fetch(0, cv);
             tmem_wait_ld();
@@ -1003,6 +1053,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
               o_col[cv.t * ostride] = o;
               tmem_wait_ld();
               if (w + 1 < ns) cv = nv;
+            }
             }
             // a chain segment that is not the last: the running state absorbs it with the fold's operations
             // (k rows from the staged rows, u rows just formed), T <- g T + k u^T node by node
