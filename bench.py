@@ -940,6 +940,9 @@ def main():
                      "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
                      "algorithmic_bytes_per_launch": r["avg_bytes"],
                      "avg_launch_ms": statistics.mean(r["verify_ms"]),
+                     # the call's spread over the K timed calls (each timed alone with CUDA events)
+                     "median_launch_ms": statistics.median(r["verify_ms"]),
+                     "min_launch_ms": min(r["verify_ms"]), "max_launch_ms": max(r["verify_ms"]),
                      "traffic": measured_traffic(w.B * w.layers),
                      "traffic_note": "DRAM bytes of the whole call (both kernels) per launch, scaled from the committed "
                                      "small-case capture (profiles/traffic_gdn_tree_verify_batched32x48.txt); null once a "
