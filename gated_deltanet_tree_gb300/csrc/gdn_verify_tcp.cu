@@ -360,6 +360,22 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       for (int s = 0; s < DK / 8; ++s) umma_tf32_ts(d, a + 8u * s, d0 + s * step, id, hi ? s > 0 : 1);
       umma_commit(b_mma);
     };
+    // wide mode: the item's Gram coefficients on the tensor cores, [G | H]^T = [K | Q] K^T over the node rows:
+    // A = the operand's first 128 rows from shared memory (k rows, then q rows: D row t holds G_t., row NB + t
+    // holds H_t.), B = its first NGc rows (the k rows), three passes for the tf32 split; D in tensor-memory
+    // columns [128, 128 + NGc), free in this mode; completion arrives on b_mma.  (For NB < 64 the rows past
+    // 2 NB read other parts of the operand; the D rows they give are not read.)
+    auto issue_gram = [&](int NB, int NGc) {
+      const uint32_t d = tbase + 128u;
+      const uint32_t lbo = static_cast<uint32_t>(4 * NB) * 16u, base = smem_addr(opnd);
+      const uint64_t hi = umma_desc(base, lbo, 128u), lo = umma_desc(base + static_cast<uint32_t>(2 * NB) * 16u, lbo, 128u);
+      const uint64_t step = static_cast<uint64_t>((2u * lbo) >> 4);
+      const uint32_t id = umma_idesc_tf32(128, NGc);
+      for (int s = 0; s < DK / 8; ++s) umma_tf32_ss(d, hi + s * step, hi + s * step, id, s > 0);
+      for (int s = 0; s < DK / 8; ++s) umma_tf32_ss(d, hi + s * step, lo + s * step, id, 1);
+      for (int s = 0; s < DK / 8; ++s) umma_tf32_ss(d, lo + s * step, hi + s * step, id, 1);
+      umma_commit(b_mma);
+    };
     ColTile<DK> R;
     auto state_ptr = [&](const Item& x, int h) {
       return p.state + (static_cast<size_t>(x.bl) * p.Hv + h) * DK * DV + c;
@@ -393,22 +409,37 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
     };
     // wide mode: the same operand from the k rows (factor bank) and q rows (workspace) in global memory
+    // (the loads of four jobs are issued before any of their stores, so four L2 round trips overlap)
     auto build_operand_g = [&](const Item& x, int ns, int NB) {
       const size_t row0 = static_cast<size_t>(x.bl) * n_max;
-      for (int job = c; job < 2 * NB * KC; job += kPGroup) {
-        const int r = job / KC, kc = job % KC;
-        const bool isq = r >= NB;
-        const int node = isq ? r - NB : r;
-        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (node < ns)
-          x4 = __ldg(reinterpret_cast<const float4*>((isq ? p.q_in : p.k_in) + ((row0 + node) * p.Hk + x.kh) * DK) + kc);
-        float4 hi, lo;
-        hi.x = tf32_hi(x4.x); lo.x = tf32_lo(x4.x);
-        hi.y = tf32_hi(x4.y); lo.y = tf32_lo(x4.y);
-        hi.z = tf32_hi(x4.z); lo.z = tf32_lo(x4.z);
-        hi.w = tf32_hi(x4.w); lo.w = tf32_lo(x4.w);
-        *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
-        *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+      const int jobs = 2 * NB * KC;
+      for (int j0 = c; j0 < jobs; j0 += 4 * kPGroup) {
+        float4 x4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int job = j0 + u * kPGroup;
+          const int r = job / KC, kc = job % KC;
+          const bool isq = r >= NB;
+          const int node = isq ? r - NB : r;
+          x4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (job < jobs && node < ns)
+            x4[u] = __ldg(reinterpret_cast<const float4*>((isq ? p.q_in : p.k_in) + ((row0 + node) * p.Hk + x.kh) * DK) +
+                          kc);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int job = j0 + u * kPGroup;
+          if (job < jobs) {
+            const int r = job / KC, kc = job % KC;
+            float4 hi, lo;
+            hi.x = tf32_hi(x4[u].x); lo.x = tf32_lo(x4[u].x);
+            hi.y = tf32_hi(x4[u].y); lo.y = tf32_lo(x4[u].y);
+            hi.z = tf32_hi(x4[u].z); lo.z = tf32_lo(x4[u].z);
+            hi.w = tf32_hi(x4[u].w); lo.w = tf32_lo(x4[u].w);
+            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + r) * 4) = hi;
+            *reinterpret_cast<float4*>(opnd + (kc * 4 * NB + 2 * NB + r) * 4) = lo;
+          }
+        }
       }
       fence_proxy_async();
     };
@@ -484,15 +515,29 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           }
           item_ok = group_and(gid, shallow);
           if (item_ok) {
+            if (wq == 0) {   // pair offsets: an exclusive scan of the depths, lane w holding nodes w and w + 32
+              const int d0 = lane < n ? dep[lane] : 0, d1 = lane + 32 < n ? dep[lane + 32] : 0;
+              int i0 = d0, i1 = d1;
+#pragma unroll
+              for (int m = 1; m < 32; m <<= 1) {
+                const int y0 = __shfl_up_sync(FULL, i0, m), y1 = __shfl_up_sync(FULL, i1, m);
+                if (lane >= m) {
+                  i0 += y0;
+                  i1 += y1;
+                }
+              }
+              const int tot0 = __shfl_sync(FULL, i0, 31);
+              if (lane < n) coff[lane] = i0 - d0;
+              if (lane + 32 < n) coff[lane + 32] = tot0 + i1 - d1;
+              if (lane == 31) coff[n] = tot0 + i1;   // (slots past n add nothing)
+            }
+            group_sync(gid);
             for (int t = c; t < n; t += kPGroup) {
-              int o = 0;
-              for (int v = 0; v < t; ++v) o += dep[v];
-              coff[t] = o;
+              int o = coff[t];
               for (int v = parent[t]; v >= 0; v = parent[v], ++o) {
                 ranc[o] = v;
                 ptn[o] = t;
               }
-              if (t == n - 1) coff[n] = o;
             }
           } else if (c == 0) {
             device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
@@ -520,6 +565,11 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         }
       }
       group_sync(gid);
+      const bool gram_tc = WIDE && item_ok;   // (the wide Gram runs on the tensor cores during the walk check)
+      if (gram_tc) {
+        if (c == 0) issue_gram(NB, (NB + 15) & ~15);
+        armed_mma = true;
+      }
       // the epilogue visits the nodes in the schedule's walk order (depth first, a node after its parent), so
       // the u values on a node's root path are the entries of a per-column stack indexed by depth.  Lane w of
       // every warp holds walk position w: node | depth << 8 | pair offset << 16.  The order is checked: every
@@ -601,7 +651,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         item_ok = group_and(gid, good);
         if (!item_ok && c == 0) device_error(p.err, GDN_DEVERR_SCHEDULE, cur.b);
       }
-      if (item_ok) {
+      if (item_ok && !WIDE) {
         // Gram coefficients, a thread per ancestor pair (and per node for H_tt); the 16-byte chunks are read
         // in an order rotated by the job, so the threads of a warp hit distinct banks
         const int np = coff[n];
@@ -612,24 +662,46 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
           const float4* kt = reinterpret_cast<const float4*>(stg + t * DK);
           const float4* qt = reinterpret_cast<const float4*>(stg + (n_max + t) * DK);
           const float4* ks = reinterpret_cast<const float4*>(stg + s * DK);
-          // (wide mode: the rows are the operand's high + low parts, which add up to the fp32 values exactly)
-          const float4* op4 = reinterpret_cast<const float4*>(opnd);
-          auto wrow = [&](int r, int kc) {
-            const float4 h4 = op4[kc * 4 * NB + r], l4 = op4[kc * 4 * NB + 2 * NB + r];
-            return make_float4(h4.x + l4.x, h4.y + l4.y, h4.z + l4.z, h4.w + l4.w);
-          };
           float sg[2] = {0.f, 0.f}, sh[2] = {0.f, 0.f};   // two partial sums each: shorter dependency chains
 #pragma unroll 8
           for (int q = 0; q < KC; ++q) {
             const int kc = (q + job) & (KC - 1);
-            const float4 a = WIDE ? wrow(t, kc) : kt[kc], b = WIDE ? wrow(NB + t, kc) : qt[kc];
-            const float4 e = WIDE ? wrow(s, kc) : ks[kc];
+            const float4 a = kt[kc], b = qt[kc], e = ks[kc];
             sg[q & 1] += fmaf(a.x, e.x, a.y * e.y) + fmaf(a.z, e.z, a.w * e.w);
             sh[q & 1] += fmaf(b.x, e.x, b.y * e.y) + fmaf(b.z, e.z, b.w * e.w);
           }
           if (diag) hd[t] = sh[0] + sh[1];
           else gh[job] = make_float2(sg[0] + sg[1], sh[0] + sh[1]);
         }
+      }
+      if (gram_tc) {
+        // wide mode: thread c reads D row c (G row of node c, or H row of node c - NB) 16 columns at a time into
+        // its own 16 words of the (here unused) depth stack, and picks its node's ancestor pairs from them
+        ok = group_and(gid, mbar_wait_ab(b_mma, ph_mma, abortw));
+        if (!ok) break;
+        ph_mma ^= 1;
+        armed_mma = false;
+        tmem_fence_after();
+        const bool isH = c >= NB;
+        const int t = isH ? c - NB : c;
+        const bool valid = item_ok && c < 2 * NB && t < n;
+        const int i0 = valid ? coff[t] : 0, dt = valid ? dep[t] : 0;
+        float* scr = stk + c * 16;
+        for (int j = 0; j < ((NB + 15) & ~15); j += 16) {
+          float v[16];
+          tmem_ld16(tA + 128u + static_cast<uint32_t>(j), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) *reinterpret_cast<float4*>(scr + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+          if (valid) {
+            for (int m = 0; m < dt; ++m) {
+              const int s2 = ranc[i0 + m];
+              if (s2 >= j && s2 < j + 16) reinterpret_cast<float*>(gh + i0 + m)[isH ? 1 : 0] = scr[s2 - j];
+            }
+            if (isH && t >= j && t < j + 16) hd[t] = scr[t - j];
+          }
+        }
+        tmem_fence_before();
       }
       fence_proxy_async();   // staging reads done before the next item's copies overwrite it
       group_sync(gid);
