@@ -286,15 +286,16 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int32_t B, int32_t layers, int32_t
  *              bits: GDN_ERR_INVALID_ARG).  By default the nodes are solved in the tree-masked
  *              UT form (article "状态驻留验证": the topology-masked UT decomposition): the
  *              committed state times every node's k and q, with no dependency between nodes,
- *              then a substitution over ancestor pairs.  Where dv = 128 and n_max <= 32 those
- *              products and the nodes' Gram rows run on the tensor cores (tcgen05, tf32 split
- *              in three for fp32 accuracy); elsewhere, or with GDN_VERIFY_UT_SIMT, on the CUDA
- *              cores.  GDN_VERIFY_CHAIN_WALK walks the packed ops instead: heavy-light chains
+ *              then a substitution over ancestor pairs.  Where dv = 128 and n_max <= 32, or
+ *              dk is 64 or 128, n_max <= 64 and sched->depth_max <= 16, those products (and
+ *              for the larger trees the nodes' Gram rows) run on the tensor cores (tcgen05, tf32
+ *              split in three for fp32 accuracy); elsewhere, or with GDN_VERIFY_UT_SIMT, on the
+ *              CUDA cores.  GDN_VERIFY_CHAIN_WALK walks the packed ops instead: heavy-light chains
  *              in registers, branch states stashed in tensor memory.  All give the same results
  *              up to rounding.  Batches whose sched->depth_max exceeds GDN_UT_MAX_DEPTH walk
  *              chains without the flag: the UT form's per-node work grows with the square of
  *              the depth.  GDN_VERIFY_CHAINS (the caller guarantees that every tree is a chain)
- *              solves chains of up to 64 nodes in the chunked UT form instead (SpecLA article,
+ *              solves chains of up to 64 nodes (dk 64 or 128) in the chunked UT form instead (SpecLA article,
  *              "想深入源码": the chunked Gated DeltaNet form): each 16-node segment is solved
  *              from the running state on the tensor cores, which then absorbs the segment with
  *              the fold's operations.
