@@ -157,9 +157,11 @@ struct PLayout {
   __host__ __device__ int stg() const { return opnd() + 4 * nbm() * dk * 4; }         // [2][n_max][dk] k, q rows
   __host__ __device__ int vbuf() const { return stg() + (mode == 2 ? 0 : 2 * n_max * dk * 4); }   // [n_max][128] v, u
   __host__ __device__ int stk() const { return vbuf() + n_max * kPDv * 4; }           // [depths][128] u by depth
-  __host__ __device__ int pk() const { return stk() + depths() * kPDv * 4; }          // [kPFold][dk] pending k
-  __host__ __device__ int pu() const { return pk() + kPFold * dk * 4; }               // [kPFold][128] pending u
-  __host__ __device__ int ptab() const { return pu() + kPFold * kPDv * 4; }           // [pairs] (A, C, s dv, -)
+  // pending rows: [pbufs][kPFold][dk] k and [pbufs][kPFold][128] u (chain mode: two buffers, a chunk ahead)
+  __host__ __device__ int pbufs() const { return mode == 1 ? 2 : 1; }
+  __host__ __device__ int pk() const { return stk() + depths() * kPDv * 4; }
+  __host__ __device__ int pu() const { return pk() + pbufs() * kPFold * dk * 4; }
+  __host__ __device__ int ptab() const { return pu() + pbufs() * kPFold * kPDv * 4; }   // [pairs] (A, C, s dv, -)
   __host__ __device__ int hsc() const { return ptab() + a16(pairs() * 16); }          // [n_max] (g, beta, bG, G)
   __host__ __device__ int gh() const { return hsc() + n_max * 16; }                   // [pairs] (G_ts, H_ts)
   __host__ __device__ int hd() const { return gh() + a16(pairs() * 8); }              // [n_max] H_tt
@@ -301,15 +303,15 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       armed_rows = true;
     };
     // pending rows f0 .. f0 + fn of v-head h; `pe` is this lane's path entry f0 + lane (warp 0)
-    auto issue_pend = [&](const Item& x, int h, int fn, int pe) {
+    auto issue_pend = [&](const Item& x, int h, int fn, int pe, int buf) {
       if (fn <= 0) return;
       if (wq == 0) {
         if (lane == 0) mbar_expect(b_pend, static_cast<uint32_t>(fn * (DK + DV) * 4));
         __syncwarp();
         if (lane < fn) {
           const size_t row = static_cast<size_t>(x.bl) * n_max + (pe & kPathNodeMask);
-          bulk_g2s(pk + lane * DK, p.pend_k + (row * p.Hk + x.kh) * DK, DK * 4, b_pend);
-          bulk_g2s(pu + lane * DV, p.pend_u + (row * p.Hv + h) * DV, DV * 4, b_pend);
+          bulk_g2s(pk + (buf * kPFold + lane) * DK, p.pend_k + (row * p.Hk + x.kh) * DK, DK * 4, b_pend);
+          bulk_g2s(pu + (buf * kPFold + lane) * DV, p.pend_u + (row * p.Hv + h) * DV, DV * 4, b_pend);
         }
       }
       armed_pend = true;
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       load_item_regs(cur);
       issue_rows(cur, cur.h0);
       const int lp0 = lp_nx > 0 ? lp_nx : 0;
-      issue_pend(cur, cur.h0, min(kPFold, lp0), pth_nx);   // (warp 0: c = lane, entry c)
+      issue_pend(cur, cur.h0, min(kPFold, lp0), pth_nx, 0);   // (warp 0: c = lane, entry c)
       load_head_regs(cur, cur.h0, lp0, pth_nx);
       R.load(state_ptr(cur, cur.h0), DV);
       prefetch_ahead(k, 0, 1);
@@ -734,26 +736,34 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
 
         // ---- 1. fold of the pending path (the chain kernel's element operations and materialisation points)
         float gam = 1.f;
-        for (int f0 = 0; f0 < Lp; f0 += kPFold) {
+        for (int f0 = 0, fb = 0; f0 < Lp; f0 += kPFold, fb ^= (L.pbufs() - 1)) {
           const int fn = min(kPFold, Lp - f0);
           ok = group_and(gid, mbar_wait_ab(b_pend, ph_pend, abortw));
           if (!ok) break;
           ph_pend ^= 1;
           armed_pend = false;
+          // chain mode: the next chunk into the other buffer now, while this one folds (its last reader, the
+          // chunk before, has finished: the barrier below closed it)
+          if (CHAIN && f0 + kPFold < Lp) {
+            const int pe = f0 + kPFold + lane < n_max ? spath[f0 + kPFold + lane] : 0;
+            issue_pend(cur, h, min(kPFold, Lp - f0 - kPFold), pe, fb ^ 1);
+          }
           if (item_ok) {
+            const float* pkb = pk + fb * kPFold * DK;
+            const float* pub = pu + fb * kPFold * DV;
             for (int i = 0; i < fn; ++i) {
               if (spath[f0 + i] & kPathHeadFlag) {
                 R.materialise(gam);
                 gam = 1.f;
               }
-              gam = fold_node(R, pk + i * DK, gam * pgt[f0 + i], pu[i * DV + c]);
+              gam = fold_node(R, pkb + i * DK, gam * pgt[f0 + i], pub[i * DV + c]);
             }
           }
           fence_proxy_async();
           group_sync(gid);
-          if (f0 + kPFold < Lp) {
+          if (!CHAIN && f0 + kPFold < Lp) {
             const int pe = f0 + kPFold + lane < n_max ? spath[f0 + kPFold + lane] : 0;
-            issue_pend(cur, h, min(kPFold, Lp - f0 - kPFold), pe);
+            issue_pend(cur, h, min(kPFold, Lp - f0 - kPFold), pe, 0);
           }
         }
         if (!ok) break;
@@ -762,7 +772,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
         // the pending buffers are free: the next head's first chunk
         if (has_nx) {
           const int pe = nx_same ? (lane < n_max ? spath[lane] : 0) : pth_nx;   // (warp 0: c = lane)
-          issue_pend(nxi, nxh, min(kPFold, nx_lp), pe);
+          issue_pend(nxi, nxh, min(kPFold, nx_lp), pe, 0);
         }
 
         if constexpr (MODE == 0) {
