@@ -411,14 +411,14 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
       fence_proxy_async();   // the operand is read by the tensor cores after the next barrier
     };
     // wide mode: the same operand from the k rows (factor bank) and q rows (workspace) in global memory
-    // (the loads of four jobs are issued before any of their stores, so four L2 round trips overlap)
+    // (the loads of eight jobs are issued before any of their stores, so eight L2 round trips overlap)
     auto build_operand_g = [&](const Item& x, int ns, int NB) {
       const size_t row0 = static_cast<size_t>(x.bl) * n_max;
       const int jobs = 2 * NB * KC;
-      for (int j0 = c; j0 < jobs; j0 += 4 * kPGroup) {
-        float4 x4[4];
+      for (int j0 = c; j0 < jobs; j0 += 8 * kPGroup) {
+        float4 x4[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int job = j0 + u * kPGroup;
           const int r = job / KC, kc = job % KC;
           const bool isq = r >= NB;
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(NG * kPGroup, 1) ut_tcp_verify_kernel(VerifyPa
                           kc);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int job = j0 + u * kPGroup;
           if (job < jobs) {
             const int r = job / KC, kc = job % KC;
