@@ -9,6 +9,7 @@ slip in the oracle -- a dropped gate, a wrong sign, a transposed state, a wrong
 tap order, a wrong GQA map, a sibling leaking into the window -- fails one of
 them.
 """
+import dataclasses
 import itertools
 import os
 
@@ -138,10 +139,11 @@ def test_hand_fixture_delta_rule():
 # projections: conv, activation, normalisation, head split
 # ---------------------------------------------------------------------------
 
-def test_conv_window_is_causal_convolution():
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 8])
+def test_conv_window_is_causal_convolution(K):
     # along a sequence, y_t = sum_j w[j] X[t-K+1+j]  ==  np.convolve(seq, w[::-1]) at position t
     rng = _rng(7)
-    K, C, L = 4, 5, 9
+    C, L = 5, 9
     w = rng.normal(size=(C, K))
     seq = rng.normal(size=(K - 1 + L, C))
     for t in range(L):
@@ -292,8 +294,9 @@ def _sequential_gdn(T, W, X, BETA, LOGG, cw, d):
     return np.array(outs), np.array([s.T for s in S_])
 
 
-def test_chain_tree_equals_sequential_gdn():
-    d, rng = D_CONV, _rng(9)
+@pytest.mark.parametrize("K", [1, 2, 4, 8])
+def test_chain_tree_equals_sequential_gdn(K):
+    d, rng = dataclasses.replace(D_CONV, K=K), _rng(9)
     n = 7
     T, W, X, BETA, LOGG, cw = _rand_inputs(d, n, rng)
     res = O.verify_tree(T, W, S.chain_tree(n), X, BETA, LOGG, cw, d)
@@ -304,7 +307,8 @@ def test_chain_tree_equals_sequential_gdn():
     sess.commit(S.chain_tree(n), list(range(n)), X, BETA, LOGG)
     Tc, Wc = sess.committed()
     np.testing.assert_allclose(Tc, T_seq, atol=1e-11)
-    np.testing.assert_array_equal(Wc, np.vstack([W, X])[-(d.K - 1):])
+    seq = np.vstack([W, X])
+    np.testing.assert_array_equal(Wc, seq[len(seq) - (d.K - 1):])   # the last K-1 raw rows (none for K = 1)
 
 
 def test_siblings_never_see_each_other():
