@@ -412,6 +412,17 @@ def reduce_across_ranks(ms: float, units: float, e2e_ms: float, e2e_units: float
     return float(t[0]), float(u[0]), float(t[1]), float(u[1])
 
 
+def zero_copy_acceptances(paths) -> dict:
+    """Accepted paths already in bank-slot order (path[i] == i for every i, the empty path included): the
+    acceptances that a fold reading the bank in path order takes without a compaction copy.  This library's
+    fold gathers the pending rows by node index, so no acceptance needs the copy; the fraction says how often
+    one would without that."""
+    paths = [list(p) for p in paths]
+    zc = sum(all(int(v) == i for i, v in enumerate(p)) for p in paths)
+    return {"fraction": zc / len(paths) if paths else None, "paths": len(paths), "zero_copy": zc,
+            "mean_length": sum(len(p) for p in paths) / len(paths) if paths else None}
+
+
 def rank_plan_trees(w: S.Workload, rank: int):
     """Every rank serves its own requests: request ids are offset by rank * B."""
     trees = [[S.tree_for(w, b + rank * w.B, s) for b in range(w.B)] for s in range(w.steps)]
@@ -982,6 +993,9 @@ def main():
             ut_speedup=r["ab"]["ms_per_step"] / (r["ms"] / args.steps)),
         "per_config": per_config,
         "cpu_baseline": cpu,
+        # rank 0's accepted paths over the workload's step cycle
+        "zero_copy_acceptances": zero_copy_acceptances(
+            [p for step in rank_plan_trees(w, 0)[1] for p in step]),
     }
     print(json.dumps(line))
 

@@ -123,3 +123,43 @@ def test_traffic_record_roundtrip(tmp_path, monkeypatch):
     src = dict(bench.KERNEL_SOURCES)
     monkeypatch.setattr(bench, "KERNEL_SOURCES", dict(src, conv_window_kernel=["gdn_commit.cu"]))
     assert bench.measured_traffic(8) is None
+
+
+def test_zero_copy_acceptances():
+    import bench
+    r = bench.zero_copy_acceptances([[0, 1, 2], [0, 2], [], [0], [0, 1, 3]])
+    assert r == {"fraction": 0.6, "paths": 5, "zero_copy": 3, "mean_length": 1.8}
+    # the batched workload's cycle: 32 requests x 8 steps, some but not all paths in slot order
+    w = bench.S.workload(4)
+    r = bench.zero_copy_acceptances([p for step in bench.rank_plan_trees(w, 0)[1] for p in step])
+    assert r["paths"] == w.B * w.steps and 0 < r["fraction"] < 1
+
+
+def test_bench_line_contract_with_a_stand_in_gpu_leg(monkeypatch, capsys):
+    # main() assembles the JSON line from the GPU leg's figures; a stand-in for that leg (no device here) checks
+    # the line's keys and the arithmetic between them
+    w = S.workload(4)
+    steps = 3
+    fake = dict(ms=15.0, units=3.0e6, verify_ms=[4.8, 4.9, 5.0], finish_ms=1.5, clocks={"sm_mhz": 2070.0},
+                ab=None, walk=None, simt=None, tc1=None, bout=None, avg_tflops=5.0e11, achieved=3000.0,
+                peak=6781.8, peak_kind="measured", avg_bytes=1.44e10, e2e_ms=16.0, avg_flops=8.0e9,
+                alu_peak=80.5, avg_verify_s=4.9e-3, e2e_units=3.0e6,
+                e2e=dict(ms=16.0, units=3.0e6, steps=steps, h2d=100, d2h=200, step_ms_median=5.3,
+                         step_ms_max=6.0, stalled_steps=0),
+                nb_cap=0, walked=False, gpu_launches=3 * steps)
+    monkeypatch.setattr(bench, "run_gpu", lambda args, w_, rank, world: fake)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--no-cpu-baseline", "--no-per-config", "--steps", str(steps),
+                                     "--warmup", "3"])
+    bench.main()
+    line = __import__("json").loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["metric"] == bench.METRIC and line["unit"] == "nodes/s" and line["n_gpus"] == 1
+    assert line["value"] == pytest.approx(3.0e6 / 15.0e-3)
+    assert line["ms_per_step"] == pytest.approx(5.0)
+    r = line["roofline"]
+    assert r["frac"] == pytest.approx(3000.0 / 6781.8) and r["bound"] in ("hbm", "alu")
+    assert r["avg_launch_ms"] == pytest.approx(4.9) and r["median_launch_ms"] == pytest.approx(4.9)
+    assert line["e2e"]["value"] == pytest.approx(3.0e6 / 16.0e-3)
+    assert line["e2e"]["h2d_bytes_per_step"] == 100 and line["e2e"]["d2h_bytes_per_step"] == 200
+    assert line["gpu_launches"] == 9 and line["clocks"] == {"sm_mhz": 2070.0}
+    assert line["config"]["requests_per_gpu"] == w.B and line["config"]["gdn_layers"] == w.layers
+    assert line["zero_copy_acceptances"]["paths"] == w.B * w.steps
