@@ -380,8 +380,9 @@ def oracle_throughput(w: S.Workload, target_s: float = 15.0, cores=None, warmup:
 
 
 def cpu_baselines(w: S.Workload, seconds: float):
-    """The oracle on 1 thread and on all host cores: configs 1-3 in full (one verify call each), and a sample
-    of the headline workload across its whole cycle.  Run before the first GPU call of the process."""
+    """The oracle on 1 thread and on all host cores: configs 1-3 in full (one verify call each), a sample of
+    the headline workload across its whole cycle, and on all cores a sample of each stress configuration
+    (64-node top-8 trees, 64-node chains) across its cycle.  Run before the first GPU call of the process."""
     ncores = os.cpu_count() or 1
     main_all = oracle_throughput(w, target_s=seconds, cores=ncores, all_steps=True)
     main_one = oracle_throughput(w, target_s=seconds * 0.6, cores=1, all_steps=True)
@@ -392,6 +393,10 @@ def cpu_baselines(w: S.Workload, seconds: float):
         allc = oracle_throughput(wc, cores=ncores, full=True)
         per[str(cfg)] = {"workload": wc.name, "one_thread": {k: one[k] for k in ("value", "seconds", "sample")},
                          "all_cores": {k: allc[k] for k in ("value", "seconds", "sample", "cores")}}
+    for cfg, key in ((5, "5(i)"), (6, "5(ii)")):   # the stress configs: a seeded sample across their cycle
+        wc = S.workload(cfg)
+        allc = oracle_throughput(wc, target_s=seconds / 3, cores=ncores, all_steps=True)
+        per[key] = {"workload": wc.name, "all_cores": {k: allc[k] for k in ("value", "seconds", "sample", "cores")}}
     out = dict(main_all)
     out["nproc"] = ncores
     out["one_thread"] = {k: main_one[k] for k in ("value", "seconds", "sample", "cores")}
