@@ -15,9 +15,9 @@
 // that loads the library, held until the process exits.
 //
 // The array is shared by every call.  The conv-window kernel writes every
-// scratch row the verify kernel of the same call later reads (rows of nodes
-// beyond a tree's size are never read), so nothing needs clearing between
-// calls; but
+// scratch row the verify kernel of the same call later uses (rows of nodes
+// beyond a tree's size may be copied along but are never used), so nothing
+// needs clearing between calls; but
 // two calls whose kernels overlap on the GPU (different streams, or different
 // host threads on one device) race on the same array and must be serialised
 // by the caller.
